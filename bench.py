@@ -1,0 +1,377 @@
+"""Benchmark of one MoE-layer forward (route -> dispatch -> grouped SwiGLU GEMM
+-> combine) on GB300, printing one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config mid]
+                    [--impl ours|reference] [--schedule interleaved|wave]
+
+A step is one moe_layer_forward over one batch of T synthetic tokens with the
+expert weights resident in HBM; L2 is flushed (a 256 MiB write) before every
+timed step, outside the timed events. Under torchrun each rank runs its own
+replica of the layer on its own tokens (weak scaling, no collective on the
+data path); rank 0 prints the max-over-ranks timing.
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on a
+bounded sample of the same workload (there is no other implementation of this
+path to run).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and TFLOP/s on 1 GB300; fraction of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 7  # route, count, scan, rank, copy, grouped GEMM, combine
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="mid", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--schedule", default="interleaved", choices=["interleaved", "wave"])
+    ap.add_argument("--lead", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(cfg, schedule):
+    return {
+        "workload": f"{cfg.name} MoE layer: T={cfg.T}, d={cfg.d}, E={cfg.E}, top_k={cfg.k}, "
+                    f"SwiGLU ffn={cfg.F}, segments={cfg.S}, "
+                    + (f"Zipf({cfg.zipf_s}) logit bias" if cfg.zipf_s else "balanced routing"),
+        "T": cfg.T, "d": cfg.d, "E": cfg.E, "top_k": cfg.k, "ffn": cfg.F, "segments": cfg.S,
+        "zipf_s": cfg.zipf_s, "seed": 0, "schedule": schedule,
+        "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+    }
+
+
+# ----------------------------------------------------------------- clocks
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        self.t0 = time.time()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]),
+                                     power=float(parts[3]) if parts[3] not in ("", "[N/A]") else None,
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] is None or r["power"] > 0] or rows
+        top = max(r["sm"] for r in busy)
+        load = [r for r in busy if r["sm"] >= 0.5 * top] or busy
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max((r["power"] or 0.0) for r in rows)}
+
+
+# ----------------------------------------------------------------- oracle leg
+def oracle_sample(cfg, inp_host, n_tokens, nthreads):
+    """The fp64 oracle on the first n tokens of the workload: route, dispatch,
+    expert FFN and combine. Returns elapsed seconds."""
+    import oracle
+
+    xb, wrb, bias, w1, w3, w2 = inp_host
+    t0 = time.perf_counter()
+    r = oracle.route(xb[:n_tokens], wrb, bias, cfg.k, nthreads=nthreads)
+    oracle.dispatch(r.idx, cfg.E)
+    oracle.layer_tokens(xb[:n_tokens], r.idx, r.gate, w1, w3, w2, np.arange(n_tokens, dtype=np.int32),
+                        cfg.E, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def host_inputs(cfg, inp=None):
+    if inp is None:
+        inp = synth.make_inputs(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    b = synth.bf16_bits
+    bias = None if inp.bias is None else inp.bias.cpu().numpy()
+    return b(inp.x), b(inp.wr), bias, b(inp.w1), b(inp.w3), b(inp.w2)
+
+
+def pick_sample_tokens(cfg, inp_host, nthreads, budget_s):
+    probe = min(cfg.T, max(2, nthreads))
+    t = oracle_sample(cfg, inp_host, probe, nthreads)
+    per_tok = t / probe
+    return int(max(probe, min(cfg.T, budget_s / max(per_tok, 1e-9)))), per_tok
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, cfg):
+    """--impl reference: the oracle, as it stands, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    nth = cpu_threads()
+    inp_host = host_inputs(cfg)
+    total_steps = args.steps + args.warmup
+    budget = min(8.0, 150.0 / max(total_steps, 1))  # the whole run stays within a few minutes
+    n, _ = pick_sample_tokens(cfg, inp_host, nth, budget)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, inp_host, n, nth)
+    times = [oracle_sample(cfg, inp_host, n, nth) for _ in range(args.steps)]
+    tsum = sum(times)
+    value = n * args.steps / tsum
+    sample = (f"first {n} of {cfg.T} tokens per step through route, dispatch, SwiGLU FFN and "
+              f"combine (fp64 oracle)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * cfg.T / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(cfg, "n/a"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our leg
+def traffic_record(cfg_name):
+    """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if its
+    kernel source still matches."""
+    p = os.path.join(ROOT, "profiles", f"grouped_gemm_{cfg_name}_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "grouped_gemm_softmax_gb300", "csrc", "grouped_gemm.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if rec.get("kernel_sha256") != h:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_ours(args, cfg):
+    import grouped_gemm_softmax_gb300 as moe
+    from grouped_gemm_softmax_gb300 import build as moe_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not moe_build.up_to_date():
+        moe_build.build()
+    moe.library()
+
+    shape = moe.Shape(T=cfg.T, d=cfg.d, E=cfg.E, top_k=cfg.k, ffn=cfg.F, num_segments=cfg.S)
+    inp = synth.make_inputs(cfg, seed=0, device=dev)
+    if rank > 0:  # each replica routes its own tokens
+        inp.x = synth.gaussian_bf16((cfg.T, cfg.d), 1.0, rank, synth.TID_X, dev)
+    ws = moe.alloc_workspace(shape, dev)
+    rows = cfg.T // cfg.S
+    out = [torch.empty(rows, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    tuning = moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE if args.schedule == "wave"
+                        else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        moe.layer_forward(shape, inp.x, inp.wr, inp.bias, inp.w1, inp.w3, inp.w2, out, ws,
+                          tuning=tuning, stage_events=evs)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    st = moe.last_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} {moe.last_device_detail()}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for evs in events:  # create the CUDA events
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step(events[k])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    st = moe.last_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} {moe.last_device_detail()}")
+
+    stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(4)] for evs in events])
+    step_ms = stage_ms.sum(1)
+    total_ms = float(step_ms.sum())
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * cfg.T * args.steps / (total_ms / 1000.0)
+    ms_per_step = total_ms / args.steps
+
+    # e2e through the same C call with host buffers: pinned H2D of x, D2H of out
+    e2e = None
+    if not args.no_e2e:
+        x_host = inp.x.cpu().pin_memory()
+        out_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+        e2e_ms = []
+        for k in range(args.warmup + args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            inp.x.copy_(x_host, non_blocking=True)
+            step()
+            for s in range(cfg.S):
+                out_host[s * rows:(s + 1) * rows].copy_(out[s], non_blocking=True)
+            b.record(stream)
+            if k >= args.warmup:
+                e2e_ms.append((a, b))
+        torch.cuda.synchronize(dev)
+        e2e_total = sum(a.elapsed_time(b) for a, b in e2e_ms)
+        if dist:
+            t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_total = float(t.item())
+        e2e = {"value": world * cfg.T * args.steps / (e2e_total / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    gemm_ms = float(stage_ms[:, 2].mean())
+    gemm_flops = cfg.gemm_flops()
+    achieved = gemm_flops / (gemm_ms / 1000.0) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = traffic_record(cfg.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": "grouped_swiglu_gemm",
+                "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s"}
+    hbm = float(peaks["hbm_gbs"])
+    t_roof = max(cfg.flops() / (peak * 1e12), cfg.minimal_bytes() / (hbm * 1e9))
+    layer_frac = t_roof / (ms_per_step / 1000.0)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        nth = cpu_threads()
+        inp_host = host_inputs(cfg, inp)
+        n, _ = pick_sample_tokens(cfg, inp_host, nth, 10.0)
+        el = oracle_sample(cfg, inp_host, n, nth)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+               "sample": f"first {n} of {cfg.T} tokens through route, dispatch, SwiGLU FFN and combine "
+                         f"(fp64 oracle, {el:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(cfg, args.schedule),
+        "tflops": cfg.flops() / (ms_per_step / 1000.0) / 1e12 * world,
+        "layer_roofline_frac": layer_frac,
+        "stage_ms": {"route": float(stage_ms[:, 0].mean()), "dispatch": float(stage_ms[:, 1].mean()),
+                     "grouped_gemm": gemm_ms, "combine": float(stage_ms[:, 3].mean())},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks,
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

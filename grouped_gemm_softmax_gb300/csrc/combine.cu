@@ -1,0 +1,90 @@
+// combine.cu -- steps 4-5 of the MoE forward, combine and weighted sum (Cui et
+// al., "Fine-grained Computation-Communication Overlap ...", section 2.1: the
+// expert outputs return to their token and the layer output is their
+// gate-weighted sum; Xian et al., "X-Stage ...", section 2.2).
+//
+//   out[t] = bf16( sum_j gate[t,j] * y_perm[row_of_slot[t*k+j]] )   (fp32, j order)
+//
+// Token t belongs to simulated source rank s = t / (T/S) and is written to row
+// t mod (T/S) of that rank's segment, the owner-aligned layout a multi-GPU
+// combine would send as one contiguous block per rank.
+//
+// One warp per token; each lane owns 16-byte column vectors (8 bf16), loads the
+// k expert rows with 128-bit loads and accumulates in fp32.
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+struct Segments {
+    uint16_t *p[kMaxSegments];
+};
+
+__device__ __forceinline__ void acc_bf16x8(float (&acc)[8], const uint4 &v, float g)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        acc[2 * h] = fmaf(g, __uint_as_float(w[h] << 16), acc[2 * h]);
+        acc[2 * h + 1] = fmaf(g, __uint_as_float(w[h] & 0xFFFF0000u), acc[2 * h + 1]);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ gate,
+               const int32_t *__restrict__ row_of_slot, int T, int d, int k, int rows_per_seg,
+               const Segments seg)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long t = static_cast<long>(blockIdx.x) * (kThreads / 32) + warp;
+    if (t >= T) return;
+    int rows[kMaxTopK];
+    float g[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        rows[j] = j < k ? row_of_slot[t * k + j] : -1;
+        g[j] = j < k ? gate[t * k + j] : 0.0f;
+    }
+    uint16_t *dst = seg.p[t / rows_per_seg] + (t % rows_per_seg) * static_cast<long>(d);
+    const int nvec = d / 8;
+    for (int v = lane; v < nvec; v += 32) {
+        uint4 val[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (rows[j] >= 0)
+                val[j] = reinterpret_cast<const uint4 *>(y + static_cast<long>(rows[j]) * d)[v];
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (rows[j] >= 0) acc_bf16x8(acc, val[j], g[j]);
+        uint4 o;
+        o.x = pack2(acc[0], acc[1]);
+        o.y = pack2(acc[2], acc[3]);
+        o.z = pack2(acc[4], acc[5]);
+        o.w = pack2(acc[6], acc[7]);
+        reinterpret_cast<uint4 *>(dst)[v] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s)
+{
+    if (a.T == 0) return cudaSuccess;
+    Segments seg;
+    for (int i = 0; i < kMaxSegments; ++i) seg.p[i] = i < a.S ? a.seg[i] : nullptr;
+    const unsigned blocks = static_cast<unsigned>((a.T + kThreads / 32 - 1) / (kThreads / 32));
+    combine_kernel<<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S,
+                                              seg);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

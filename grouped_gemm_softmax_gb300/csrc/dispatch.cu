@@ -1,0 +1,186 @@
+// dispatch.cu -- step 2 of the MoE forward, dispatch (Cui et al., "Fine-grained
+// Computation-Communication Overlap ...", section 2.1 step 2): every token copy
+// (t, j) goes to a row of its expert's contiguous block, stable in (t, j)
+// order, and its hidden vector is copied there.
+//
+// Four kernels, all deterministic (no atomics whose order decides a result):
+//   1. count   one block per chunk of C tokens: per-expert counts of its slots
+//   2. scan    one block: per expert, exclusive scan over chunks, then over
+//              experts -> expert_counts, expert_offsets, and each chunk's
+//              first row per expert; also clears the grouped GEMM's counters
+//   3. rank    one block per chunk: warp 0 walks the chunk's slots in order,
+//              32 at a time, ranking equal experts with __match_any_sync, and
+//              writes row_of_slot / slot_of_row
+//   4. copy    one warp per token: x[t] read once with 16-byte loads and
+//              written to its k destination rows
+#include "kernels.cuh"
+#include "sm100.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kScanMaxCells = 8192;  // chunks * E held in shared memory by the scan
+constexpr int kRankBatch = 2048;      // slots staged in shared memory per pass
+
+__global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restrict__ idx, int T, int k,
+                                                         int E, int C, int32_t *chunk_base,
+                                                         unsigned *status)
+{
+    __shared__ int cnt[kMaxExperts];
+    for (int e = threadIdx.x; e < E; e += kThreads) cnt[e] = 0;
+    __syncthreads();
+    const long s0 = static_cast<long>(blockIdx.x) * C * k;
+    const long s1 = min(static_cast<long>(T), static_cast<long>(blockIdx.x + 1) * C) * k;
+    for (long s = s0 + threadIdx.x; s < s1; s += kThreads) {
+        const int e = idx[s];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else report_failure(status, kStatusBadExpert, kWhereDispatch, static_cast<unsigned>(s));
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads)
+        chunk_base[static_cast<long>(blockIdx.x) * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(kThreads) scan_kernel(int32_t *chunk_base, int nchunks, int E,
+                                                        int32_t *counts, int32_t *offsets,
+                                                        unsigned *zero_words, long zero_count)
+{
+    __shared__ int cells[kScanMaxCells];
+    __shared__ int tot[kMaxExperts];
+    __shared__ int warp_sums[kThreads / 32];
+    const int n = nchunks * E;
+    for (int i = threadIdx.x; i < n; i += kThreads) cells[i] = chunk_base[i];
+    __syncthreads();
+    // per expert: exclusive scan over chunks (in chunk order)
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int v = cells[c * E + e];
+            cells[c * E + e] = run;
+            run += v;
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+    // exclusive scan over experts (E <= 256 = kThreads)
+    const int e = threadIdx.x;
+    const int v = e < E ? tot[e] : 0;
+    const int lane = e & 31, w = e >> 5;
+    int incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < w; ++i) before += warp_sums[i];
+    const int excl = before + incl - v;
+    if (e < E) {
+        counts[e] = v;
+        offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + v;
+        tot[e] = excl;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kThreads) chunk_base[i] = cells[i] + tot[i % E];
+    for (long i = threadIdx.x; i < zero_count; i += kThreads) zero_words[i] = 0u;
+}
+
+__global__ void __launch_bounds__(kThreads) rank_kernel(const int32_t *__restrict__ idx, int T, int k,
+                                                        int E, int C,
+                                                        const int32_t *__restrict__ chunk_base,
+                                                        int32_t *row_of_slot, int32_t *slot_of_row)
+{
+    __shared__ int cur[kMaxExperts];
+    __shared__ int sidx[kRankBatch];
+    for (int e = threadIdx.x; e < E; e += kThreads)
+        cur[e] = chunk_base[static_cast<long>(blockIdx.x) * E + e];
+    const long s0 = static_cast<long>(blockIdx.x) * C * k;
+    const long s1 = min(static_cast<long>(T), static_cast<long>(blockIdx.x + 1) * C) * k;
+    const int lane = threadIdx.x & 31;
+    for (long b0 = s0; b0 < s1; b0 += kRankBatch) {
+        const int nb = static_cast<int>(min(static_cast<long>(kRankBatch), s1 - b0));
+        __syncthreads();
+        for (int i = threadIdx.x; i < nb; i += kThreads) sidx[i] = idx[b0 + i];
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const unsigned lt = (1u << lane) - 1u;
+            for (int i0 = 0; i0 < nb; i0 += 32) {
+                const int i = i0 + lane;
+                const int e0 = i < nb ? sidx[i] : -1;
+                const bool in_range = e0 >= 0 && e0 < E;
+                const bool valid = i < nb && in_range;
+                const int e = valid ? e0 : -1;
+                if (i < nb && !in_range) row_of_slot[b0 + i] = -1;
+                const unsigned peers = __match_any_sync(0xffffffffu, e);
+                const int rank = __popc(peers & lt);
+                const int base = valid ? cur[e] : 0;
+                __syncwarp();
+                if (valid) {
+                    const int row = base + rank;
+                    const long s = b0 + i;
+                    row_of_slot[s] = row;
+                    slot_of_row[row] = static_cast<int32_t>(s);
+                    if (rank == 0) cur[e] = base + __popc(peers);
+                }
+                __syncwarp();
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) copy_kernel(const uint16_t *__restrict__ x,
+                                                        const int32_t *__restrict__ row_of_slot,
+                                                        int T, int d, int k, uint16_t *x_perm)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long t = static_cast<long>(blockIdx.x) * (kThreads / 32) + warp;
+    if (t >= T) return;
+    int rows[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? row_of_slot[t * k + j] : 0;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d);
+    const int nvec = d / 8;
+    for (int v = lane; v < nvec; v += 32) {
+        const uint4 val = src[v];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k && rows[j] >= 0)
+                reinterpret_cast<uint4 *>(x_perm + static_cast<long>(rows[j]) * d)[v] = val;
+    }
+}
+
+}  // namespace
+
+int dispatch_chunk_tokens(int T, int E)
+{
+    // at most kScanMaxCells (chunk, expert) cells for the single-block scan
+    const long max_chunks = kScanMaxCells / E;
+    long c = (static_cast<long>(T) + max_chunks - 1) / max_chunks;
+    c = (c + 31) / 32 * 32;
+    return static_cast<int>(c < 256 ? 256 : c);
+}
+
+cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t s)
+{
+    if (a.T == 0) {
+        // no tokens: counts and offsets are all zero
+        cudaError_t err = cudaMemsetAsync(a.counts, 0, sizeof(int32_t) * a.E, s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(a.offsets, 0, sizeof(int32_t) * (a.E + 1), s);
+        return err;
+    }
+    const int C = a.chunk_tokens;
+    const int nchunks = (a.T + C - 1) / C;
+    count_kernel<<<nchunks, kThreads, 0, s>>>(a.topk_idx, a.T, a.k, a.E, C, a.chunk_base, a.status);
+    scan_kernel<<<1, kThreads, 0, s>>>(a.chunk_base, nchunks, a.E, a.counts, a.offsets,
+                                       a.zero_words, a.zero_words ? a.zero_count : 0);
+    rank_kernel<<<nchunks, kThreads, 0, s>>>(a.topk_idx, a.T, a.k, a.E, C, a.chunk_base,
+                                             a.row_of_slot, a.slot_of_row);
+    const unsigned copy_blocks = static_cast<unsigned>((a.T + kThreads / 32 - 1) / (kThreads / 32));
+    copy_kernel<<<copy_blocks, kThreads, 0, s>>>(a.x, a.row_of_slot, a.T, a.d, a.k, a.x_perm);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,613 @@
+// grouped_gemm.cu -- the expert computation of one MoE layer as ONE persistent
+// grouped GEMM over all experts (Xian et al., "X-Stage ...", section 2.2:
+// Linear-1 -> SwiGLU -> Linear-2 per expert; Cui et al., "Fine-grained
+// Computation-Communication Overlap ...", section 3.3.1: one rank-wide
+// persistent kernel over a unified tile worklist with per-tile ready flags).
+//
+// Tiles. Rows of x_perm are expert-contiguous. A "scheduler row" is one
+// 128-row M-tile of one expert; the scheduler rows of all experts are
+// concatenated in expert order (row p -> expert e(p), first row O_e).
+//   Linear-1 tile (p, n): h[rows, n*128 : n*128+128] =
+//       bf16(silu(x W1[e]^T) * (x W3[e]^T)); the MMA is 128 x 256 x 16 with the
+//       W1 tile stacked on the W3 tile, so one accumulator holds gate | up.
+//   Linear-2 tile (p, n): y[rows, n*N2 : n*N2+N2] = bf16(h W2[e]^T).
+// A Linear-2 tile of row p reads h rows that all Linear-1 tiles of row p write;
+// each finished Linear-1 tile increments l1_done[p] (release) and the TMA
+// producer of a Linear-2 tile waits (acquire, bounded) until it reaches P1.
+// Each finished Linear-2 tile publishes its ready flag (= the call's epoch).
+//
+// Order (Xian et al., Algorithm 1, read for unpaired CTAs): CTA g of G walks two
+// cursors k1, k2 (start g, step G) over the Linear-1 and Linear-2 tile streams
+// (row-major over (row, n)); it emits the Linear-2 tile at k2 when its row
+// trails the Linear-1 cursor's row by at least D, else the next Linear-1 tile.
+// With D >= 1 every Linear-2 tile waits only on Linear-1 tiles of earlier
+// positions in every CTA's sequence, so the waits cannot deadlock (all CTAs
+// are co-resident: grid <= SM count, one CTA per SM). The expert-wave order
+// (all Linear-1 tiles of a wave of experts, then its Linear-2 tiles) is kept
+// as the comparison schedule. Both orders give bit-identical outputs.
+//
+// CTA roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
+// allocator + single-thread MMA issuer, warps 2..5 = epilogue (warp w reads
+// tensor-memory lanes 32*(w%4)...+31). Shared memory holds a 4-stage ring of
+// (A 128x64, B 256x64) bf16 tiles in the 128-byte-swizzled K-major layout;
+// tensor memory holds two 128x256 fp32 accumulators (512 columns).
+#include <climits>
+
+#include "kernels.cuh"
+#include "sm100.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kBlockK = 64;  // 64 bf16 = 128 B = one swizzle atom row
+constexpr int kL1N = 128;    // h columns per Linear-1 tile (MMA N = 2 * 128)
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
+constexpr int kBTileBytes = 256 * kBlockK * 2;      // 32 KiB
+constexpr int kL1StageBytes = kATileBytes + kBTileBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+
+struct GemmParams {
+    const int32_t *offsets;
+    uint16_t *h;
+    uint16_t *y;
+    unsigned *l1_done;
+    unsigned *l2_flags;
+    unsigned *status;
+    int E, d, F, R;
+    int P1, P2, N2;
+    int kb1, kb2;
+    int schedule, lead;
+    unsigned epoch;
+};
+
+struct SmemCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+    int nwaves;
+    int offs[kMaxExperts + 1];       // expert row offsets (copy of expert_offsets)
+    int row_start[kMaxExperts + 1];  // first scheduler row of each expert
+    int wave_row[kMaxExperts + 1];   // wave w spans scheduler rows [wave_row[w], wave_row[w+1])
+    long wave_tile[kMaxExperts + 1]; // first global tile index of wave w
+};
+
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * (kATileBytes + kBTileBytes) +
+                              sizeof(SmemCtl);
+
+struct Tile {
+    int kind;  // 0 = Linear-1, 1 = Linear-2, -1 = no more tiles
+    int row;
+    int n;
+};
+
+// Every role of a CTA runs its own copy of this deterministic walk, so they all
+// see the same tile sequence without communicating.
+struct Scheduler {
+    long k1, k2, tot1, tot2;
+    long gi;
+    int w;
+    int P1, P2, G, D, mode;
+
+    __device__ Scheduler(const SmemCtl &c, const GemmParams &p)
+    {
+        const long P = c.row_start[p.E];
+        P1 = p.P1;
+        P2 = p.P2;
+        G = gridDim.x;
+        D = p.lead;
+        mode = p.schedule;
+        k1 = k2 = blockIdx.x;
+        tot1 = P * P1;
+        tot2 = P * P2;
+        gi = blockIdx.x;
+        w = 0;
+    }
+
+    __device__ Tile next(const SmemCtl &c)
+    {
+        Tile t;
+        if (mode == 0) {
+            if (k1 >= tot1 && k2 >= tot2) {
+                t.kind = -1;
+                return t;
+            }
+            const long p1 = (k1 < tot1) ? k1 / P1 : LONG_MAX / 2;
+            if (k2 < tot2 && k2 / P2 + D <= p1) {
+                t.kind = 1;
+                t.row = static_cast<int>(k2 / P2);
+                t.n = static_cast<int>(k2 % P2);
+                k2 += G;
+            } else {
+                t.kind = 0;
+                t.row = static_cast<int>(k1 / P1);
+                t.n = static_cast<int>(k1 % P1);
+                k1 += G;
+            }
+            return t;
+        }
+        if (gi >= c.wave_tile[c.nwaves]) {
+            t.kind = -1;
+            return t;
+        }
+        while (gi >= c.wave_tile[w + 1]) ++w;
+        long j = gi - c.wave_tile[w];
+        const int r0 = c.wave_row[w];
+        const long nr = c.wave_row[w + 1] - r0;
+        if (j < nr * P1) {
+            t.kind = 0;
+            t.row = r0 + static_cast<int>(j / P1);
+            t.n = static_cast<int>(j % P1);
+        } else {
+            j -= nr * P1;
+            t.kind = 1;
+            t.row = r0 + static_cast<int>(j / P2);
+            t.n = static_cast<int>(j % P2);
+        }
+        gi += G;
+        return t;
+    }
+};
+
+// expert owning scheduler row `row` (the last e with row_start[e] <= row)
+__device__ __forceinline__ int row_expert(const SmemCtl &c, int E, int row)
+{
+    int lo = 0, hi = E;  // row_start[lo] <= row < row_start[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (c.row_start[mid] <= row) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ bool wait_rows_ready(const unsigned *ctr, unsigned target,
+                                                volatile int *cta_abort, unsigned *status,
+                                                unsigned detail)
+{
+    if (ld_acquire_u32(ctr) >= target) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(128);
+        if (ld_acquire_u32(ctr) >= target) return true;
+        if ((it & 15u) == 0u) {
+            if (*cta_abort) return false;
+            if (ld_volatile_u32(status) != 0u) {
+                *cta_abort = 1;
+                return false;
+            }
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                report_failure(status, kStatusTimeout, kWhereProducerDep, detail);
+                *cta_abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits)
+{
+    const float g = __uint_as_float(g_bits);
+    const float u = __uint_as_float(u_bits);
+    return g / (1.0f + __expf(-g)) * u;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
+                           const __grid_constant__ CUtensorMap tm_h,
+                           const __grid_constant__ CUtensorMap tm_w1,
+                           const __grid_constant__ CUtensorMap tm_w3,
+                           const __grid_constant__ CUtensorMap tm_w2, const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+    uint8_t *sA = reinterpret_cast<uint8_t *>(base);
+    uint8_t *sB = sA + kStages * kATileBytes;
+    SmemCtl &c = *reinterpret_cast<SmemCtl *>(sB + kStages * kBTileBytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = p.E;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&c.full[s], 1);
+            mbar_init(&c.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c.tfull[b], 1);
+            mbar_init(&c.tempty[b], kEpiThreads);
+        }
+        c.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_h);
+        tma_prefetch_desc(&tm_w1);
+        tma_prefetch_desc(&tm_w3);
+        tma_prefetch_desc(&tm_w2);
+    }
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    if (warp == 2) {
+        // expert offsets -> scheduler-row prefix (warp-parallel exclusive scan).
+        // Offsets that are not a non-decreasing sequence from 0 to R are
+        // reported and leave the kernel with no tiles (nothing is written).
+        const int per = (E + 31) / 32;
+        int local = 0;
+        bool bad = false;
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e < E) {
+                const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
+                c.offs[e] = o0;
+                if (e == E - 1) c.offs[E] = o1;
+                bad |= o1 < o0 || (e == 0 && o0 != 0) || (e == E - 1 && o1 != p.R);
+                local += (o1 - o0 + kBlockM - 1) / kBlockM;
+            }
+        }
+        const bool any_bad = __any_sync(0xffffffffu, bad);
+        if (any_bad) {
+            local = 0;
+            if (lane == 0 && blockIdx.x == 0)
+                report_failure(p.status, kStatusBadOffsets, kWhereGemmOffsets, 0);
+        }
+        int incl = local;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        __syncwarp();  // offs[] written by other lanes above
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e < E) {
+                c.row_start[e] = run;
+                if (!any_bad) run += (c.offs[e + 1] - c.offs[e] + kBlockM - 1) / kBlockM;
+            }
+        }
+        if (lane == 31) c.row_start[E] = incl;
+        __syncwarp();
+        if (lane == 0) {
+            // expert waves for the comparison schedule: consecutive experts until
+            // the wave's Linear-1 tiles fill the grid once
+            int nw = 0;
+            long tiles = 0;
+            c.wave_row[0] = 0;
+            c.wave_tile[0] = 0;
+            int wr = 0;
+            for (int e = 0; e < E; ++e) {
+                const int r1 = c.row_start[e + 1];
+                if (static_cast<long>(r1 - wr) * p.P1 >= gridDim.x || e == E - 1) {
+                    tiles += static_cast<long>(r1 - wr) * (p.P1 + p.P2);
+                    ++nw;
+                    c.wave_row[nw] = r1;
+                    c.wave_tile[nw] = tiles;
+                    wr = r1;
+                }
+            }
+            c.nwaves = nw;
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = c.tmem_base;
+    volatile int *abort_flag = &c.abort;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            Scheduler sch(c, p);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            while (ok) {
+                const Tile t = sch.next(c);
+                if (t.kind < 0) break;
+                const int e = row_expert(c, E, t.row);
+                const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kBlockM;
+                if (t.kind == 1) {
+                    if (!wait_rows_ready(&p.l1_done[t.row], static_cast<unsigned>(p.P1), abort_flag,
+                                         p.status, static_cast<unsigned>(t.row)))
+                        break;
+                    fence_proxy_async_global();
+                }
+                const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
+                const uint32_t bytes =
+                    t.kind == 0 ? kL1StageBytes : kATileBytes + p.N2 * kBlockK * 2;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag, p.status, kWhereProducerEmpty,
+                                   static_cast<unsigned>(s))) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&c.full[s], bytes);
+                    uint8_t *a = sA + s * kATileBytes;
+                    uint8_t *b = sB + s * kBTileBytes;
+                    if (t.kind == 0) {
+                        tma_load_2d(&tm_x, &c.full[s], a, kb * kBlockK, row0);
+                        tma_load_3d(&tm_w1, &c.full[s], b, kb * kBlockK, t.n * kL1N, e);
+                        tma_load_3d(&tm_w3, &c.full[s], b + kBTileBytes / 2, kb * kBlockK,
+                                    t.n * kL1N, e);
+                    } else {
+                        tma_load_2d(&tm_h, &c.full[s], a, kb * kBlockK, row0);
+                        tma_load_3d(&tm_w2, &c.full[s], b, kb * kBlockK, t.n * p.N2, e);
+                    }
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            Scheduler sch(c, p);
+            int s = 0;
+            uint32_t ph = 0;
+            const uint32_t idesc1 = idesc_bf16_f32(kBlockM, 2 * kL1N);
+            const uint32_t idesc2 = idesc_bf16_f32(kBlockM, p.N2);
+            bool ok = true;
+            for (int tl = 0; ok; ++tl) {
+                const Tile t = sch.next(c);
+                if (t.kind < 0) break;
+                const int b = tl & 1;
+                const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
+                if (!mbar_wait(&c.tempty[b], aph ^ 1u, abort_flag, p.status, kWhereMmaTmemEmpty,
+                               static_cast<unsigned>(tl)))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b) * kAccCols;
+                const uint32_t idesc = t.kind == 0 ? idesc1 : idesc2;
+                const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&c.full[s], ph, abort_flag, p.status, kWhereMmaFull,
+                                   static_cast<unsigned>(s))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + s * kATileBytes));
+                    const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + s * kBTileBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                        // advance 16 bf16 (32 B) along K inside the swizzle atom
+                        mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&c.empty[s]);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(&c.tfull[b]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int r_in_tile = q * 32 + lane;
+        const bool publisher = (warp == 2 && lane == 0);
+        Scheduler sch(c, p);
+        for (int tl = 0;; ++tl) {
+            const Tile t = sch.next(c);
+            if (t.kind < 0) break;
+            const int b = tl & 1;
+            const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
+            if (!mbar_wait(&c.tfull[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
+                           static_cast<unsigned>(tl)))
+                break;
+            tc_fence_after();
+            const int e = row_expert(c, E, t.row);
+            const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kBlockM;
+            const int valid_rows = min(kBlockM, c.offs[e + 1] - row0);
+            const bool valid = r_in_tile < valid_rows;
+            const long grow = static_cast<long>(row0) + r_in_tile;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(b) * kAccCols;
+            if (t.kind == 0) {
+                for (int c32 = 0; c32 < kL1N / 32; ++c32) {
+                    uint32_t g[32], u[32];
+                    tmem_load_32cols(tbase + c32 * 32, g);
+                    tmem_load_32cols(tbase + kL1N + c32 * 32, u);
+                    const int col0 = t.n * kL1N + c32 * 32;
+                    if (valid) {
+                        uint16_t *dst = p.h + grow * p.F + col0;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 < p.F) {
+                                uint4 pk;
+                                pk.x = pack_bf16x2(silu_mul(g[v * 8 + 0], u[v * 8 + 0]),
+                                                   silu_mul(g[v * 8 + 1], u[v * 8 + 1]));
+                                pk.y = pack_bf16x2(silu_mul(g[v * 8 + 2], u[v * 8 + 2]),
+                                                   silu_mul(g[v * 8 + 3], u[v * 8 + 3]));
+                                pk.z = pack_bf16x2(silu_mul(g[v * 8 + 4], u[v * 8 + 4]),
+                                                   silu_mul(g[v * 8 + 5], u[v * 8 + 5]));
+                                pk.w = pack_bf16x2(silu_mul(g[v * 8 + 6], u[v * 8 + 6]),
+                                                   silu_mul(g[v * 8 + 7], u[v * 8 + 7]));
+                                *reinterpret_cast<uint4 *>(dst + v * 8) = pk;
+                            }
+                        }
+                    }
+                }
+            } else {
+                const int nchunks = p.N2 / 32;
+                for (int c32 = 0; c32 < nchunks; ++c32) {
+                    uint32_t a[32];
+                    tmem_load_32cols(tbase + c32 * 32, a);
+                    const int col0 = t.n * p.N2 + c32 * 32;
+                    if (valid) {
+                        uint16_t *dst = p.y + grow * p.d + col0;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 < p.d) {
+                                uint4 pk;
+                                pk.x = pack_bf16x2(__uint_as_float(a[v * 8 + 0]),
+                                                   __uint_as_float(a[v * 8 + 1]));
+                                pk.y = pack_bf16x2(__uint_as_float(a[v * 8 + 2]),
+                                                   __uint_as_float(a[v * 8 + 3]));
+                                pk.z = pack_bf16x2(__uint_as_float(a[v * 8 + 4]),
+                                                   __uint_as_float(a[v * 8 + 5]));
+                                pk.w = pack_bf16x2(__uint_as_float(a[v * 8 + 6]),
+                                                   __uint_as_float(a[v * 8 + 7]));
+                                *reinterpret_cast<uint4 *>(dst + v * 8) = pk;
+                            }
+                        }
+                    }
+                }
+            }
+            // this thread's stores before any later TMA read of them (other CTAs)
+            fence_proxy_async_global();
+            tc_fence_before();
+            mbar_arrive(&c.tempty[b]);
+            if (publisher) {
+                // all 128 epilogue threads have stored: publish the tile
+                if (mbar_wait(&c.tempty[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
+                              0x80000000u | static_cast<unsigned>(tl))) {
+                    __threadfence();
+                    if (t.kind == 0)
+                        red_release_add_u32(&p.l1_done[t.row], 1u);
+                    else
+                        st_release_u32(&p.l2_flags[static_cast<long>(t.row) * p.P2 + t.n],
+                                       p.epoch);
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+bool make_map_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                 uint32_t box_outer)
+{
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t mid, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_mid)
+{
+    const cuuint64_t dims[3] = {inner, mid, outer};
+    const cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+    const cuuint32_t box[3] = {box_inner, box_mid, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int ffn_l2_block_n(int d, int requested)
+{
+    if (requested >= 32 && requested <= 256 && requested % 32 == 0) return requested;
+    // widest tile (multiple of 32) that wastes the fewest padded columns
+    int best = 256;
+    long best_pad = LONG_MAX;
+    for (int n = 256; n >= 64; n -= 32) {
+        const long pad = static_cast<long>((d + n - 1) / n) * n - d;
+        if (pad < best_pad) {
+            best_pad = pad;
+            best = n;
+        }
+    }
+    return best;
+}
+
+long ffn_max_rows(long R, int E)
+{
+    // sum_e ceil(c_e / 128) <= R / 128 + E
+    return R / kBlockM + E + 1;
+}
+
+cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
+{
+    const long R = a.R;
+    if (R == 0) return cudaSuccess;
+    GemmParams p;
+    p.offsets = a.offsets;
+    p.h = a.h;
+    p.y = a.y;
+    p.l1_done = a.l1_done;
+    p.l2_flags = a.l2_flags;
+    p.status = a.status;
+    p.E = a.E;
+    p.d = a.d;
+    p.F = a.F;
+    p.R = a.R;
+    p.N2 = ffn_l2_block_n(a.d, a.l2_block_n);
+    p.P1 = (a.F + kL1N - 1) / kL1N;
+    p.P2 = (a.d + p.N2 - 1) / p.N2;
+    p.kb1 = (a.d + kBlockK - 1) / kBlockK;
+    p.kb2 = (a.F + kBlockK - 1) / kBlockK;
+    p.schedule = a.schedule;
+    p.epoch = a.epoch;
+
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    int grid = a.num_ctas > 0 ? a.num_ctas : sms;
+    if (grid > sms) grid = sms;
+    // minimum lead of Linear-1 over Linear-2 (scheduler rows): the Linear-1
+    // frontier of G CTAs spans about G / P1 rows, plus one row of margin
+    p.lead = a.lead > 0 ? a.lead : (grid + p.P1 - 1) / p.P1 + 1;
+
+    CUtensorMap tx, th, tw1, tw3, tw2;
+    if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, kBlockM) ||
+        !make_map_2d(&th, a.h, a.F, R, kBlockK, kBlockM) ||
+        !make_map_3d(&tw1, a.w1, a.d, a.F, a.E, kBlockK, kL1N) ||
+        !make_map_3d(&tw3, a.w3, a.d, a.F, a.E, kBlockK, kL1N) ||
+        !make_map_3d(&tw2, a.w2, a.F, a.d, a.E, kBlockK, p.N2))
+        return cudaErrorInvalidValue;
+
+    if (!a.counters_zeroed) {
+        cudaError_t err = cudaMemsetAsync(a.l1_done, 0, sizeof(unsigned) * a.max_rows, stream);
+        if (err != cudaSuccess) return err;
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kSmemBytes));
+        if (err != cudaSuccess) return err;
+        attr_set = true;
+    }
+    grouped_swiglu_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tx, th, tw1, tw3, tw2, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,81 @@
+// kernels.cuh -- host-side launch interface between the C ABI (moe_api.cu) and
+// the kernels (route.cu, dispatch.cu, grouped_gemm.cu, combine.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxSegments = 64;
+
+struct RouteArgs {
+    const uint16_t *x;       // [T,d] bf16
+    const uint16_t *wr;      // [E,d] bf16
+    const float *bias;       // [E] or null
+    int32_t *topk_idx;       // [T,k]
+    float *topk_gate;        // [T,k]
+    int T, d, E, k;
+};
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
+
+struct DispatchArgs {
+    const uint16_t *x;       // [T,d]
+    const int32_t *topk_idx; // [T,k]
+    int32_t *counts;         // [E]
+    int32_t *offsets;        // [E+1]
+    int32_t *row_of_slot;    // [R]
+    int32_t *slot_of_row;    // [R]
+    uint16_t *x_perm;        // [R,d]
+    int32_t *chunk_base;     // [nchunks,E] scratch
+    unsigned *status;        // device status words (an expert id outside [0,E) is reported here)
+    unsigned *zero_words;    // optional: words to clear for the grouped GEMM (may be null)
+    long zero_count;
+    int T, d, E, k;
+    int chunk_tokens;
+};
+int dispatch_chunk_tokens(int T, int E);
+cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t s);
+
+struct FfnArgs {
+    const uint16_t *x_perm;  // [R,d]
+    const int32_t *offsets;  // [E+1]
+    const uint16_t *w1, *w3; // [E,F,d]
+    const uint16_t *w2;      // [E,d,F]
+    uint16_t *h;             // [R,F]
+    uint16_t *y;             // [R,d]
+    unsigned *l1_done;       // [max_rows]
+    unsigned *l2_flags;      // [max_rows * P2]
+    unsigned *status;        // 4 words
+    long max_rows;
+    int R, d, F, E;
+    int schedule, lead, num_ctas, l2_block_n;
+    bool counters_zeroed;    // l1_done already cleared by an earlier kernel on the stream
+    unsigned epoch;
+};
+int ffn_l2_block_n(int d, int requested);
+long ffn_max_rows(long R, int E);
+cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s);
+
+struct CombineArgs {
+    const uint16_t *y;        // [R,d]
+    const float *gate;        // [T,k]
+    const int32_t *row_of_slot;
+    uint16_t *seg[kMaxSegments];
+    int T, d, k, S;
+};
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+
+// driver entry point for tensor-map encoding, resolved once through the runtime
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+int device_sm_count();
+
+}  // namespace moe

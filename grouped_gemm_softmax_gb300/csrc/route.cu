@@ -1,0 +1,218 @@
+// route.cu -- step 1 of the MoE forward, routing (Cui et al., "Fine-grained
+// Computation-Communication Overlap ...", section 2.1 step 1: the router picks
+// the top-k experts from a probability distribution and yields the gate
+// weights; Xian et al., "X-Stage ...", section 2.2).
+//
+//   z[t,e]        = sum_i x[t,i] * Wr[e,i]  (+ bias[e])
+//   topk_idx[t,:] = the k largest z[t,:], descending, ties to the lower index
+//   topk_gate[t,:]= softmax over those k logits
+//
+// Logits are computed on CUDA cores in fp32 (tensor cores are kept for the
+// expert GEMMs). Each logit is accumulated by ONE thread in ascending i with
+// fmaf: every bf16 x bf16 product is exact in fp32, so the result is the fp32
+// sequential sum, rounded once per addition, independent of the tiling. The
+// selection is therefore reproducible bit for bit by any implementation of
+// that sum.
+//
+// Block tile: BT = 64 tokens x BE = 8*TX experts, staged through shared memory
+// 32 features at a time (fp32, transposed), each thread owning TM tokens x 8
+// experts. Then one warp per token runs k rounds of a shuffle arg-max over the
+// block's logits and writes idx and gates.
+#include <cuda_bf16.h>
+#include <float.h>
+
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 32;
+constexpr int kTN = 8;
+
+struct RouteParams {
+    const uint16_t *x;
+    const uint16_t *wr;
+    const float *bias;
+    int32_t *idx;
+    float *gate;
+    int T, d, E, k;
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
+{
+    return __uint_as_float(bits16 << 16);
+}
+
+template <int TX, int TM, int NT>
+__global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
+{
+    constexpr int TY = NT / TX;
+    constexpr int BT = TY * TM;
+    constexpr int BE = TX * kTN;
+    constexpr int NW = NT / 32;
+    extern __shared__ float rsm[];
+    float *xs = rsm;             // [kBK][BT]
+    float *ws = rsm + kBK * BT;  // [kBK][BE]
+    float *lg = rsm;             // [BT][BE + 1] (reused after the K loop)
+
+    const int tid = threadIdx.x;
+    const int tx = tid % TX;
+    const int ty = tid / TX;
+    const long t0 = static_cast<long>(blockIdx.x) * BT;
+
+    float acc[TM][kTN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < kTN; ++j) acc[i][j] = 0.0f;
+
+    // staging: 16-byte vectors (8 features) of BT token rows and BE expert rows
+    constexpr int XV = BT * (kBK / 8);
+    constexpr int WV = BE * (kBK / 8);
+    for (int k0 = 0; k0 < p.d; k0 += kBK) {
+        for (int v = tid; v < XV; v += NT) {
+            const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
+            const long t = t0 + r;
+            uint4 q = make_uint4(0, 0, 0, 0);
+            if (t < p.T && k0 + c8 < p.d)
+                q = *reinterpret_cast<const uint4 *>(p.x + t * p.d + k0 + c8);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                xs[(c8 + 2 * h) * BT + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
+                xs[(c8 + 2 * h + 1) * BT + r] = bf16_bits_to_f32(w[h] >> 16);
+            }
+        }
+        for (int v = tid; v < WV; v += NT) {
+            const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
+            uint4 q = make_uint4(0, 0, 0, 0);
+            if (r < p.E && k0 + c8 < p.d)
+                q = *reinterpret_cast<const uint4 *>(p.wr + static_cast<long>(r) * p.d + k0 + c8);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                ws[(c8 + 2 * h) * BE + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
+                ws[(c8 + 2 * h + 1) * BE + r] = bf16_bits_to_f32(w[h] >> 16);
+            }
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < kBK; ++kk) {
+            float xv[TM], wv[kTN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) xv[i] = xs[kk * BT + ty * TM + i];
+#pragma unroll
+            for (int j = 0; j < kTN; ++j) wv[j] = ws[kk * BE + tx * kTN + j];
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < kTN; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+
+    // logits (+ bias, one fp32 addition) into shared memory
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+#pragma unroll
+        for (int j = 0; j < kTN; ++j) {
+            const int e = tx * kTN + j;
+            float z = acc[i][j];
+            if (p.bias != nullptr && e < p.E) z = z + p.bias[e];
+            lg[(ty * TM + i) * (BE + 1) + e] = z;
+        }
+    }
+    __syncthreads();
+
+    const int warp = tid / 32, lane = tid % 32;
+    for (int r = warp; r < BT; r += NW) {
+        const long t = t0 + r;
+        if (t >= p.T) break;
+        const float *row = lg + r * (BE + 1);
+        constexpr int PER = (BE + 31) / 32;
+        float v[PER];
+        uint32_t avail = 0;  // bit i: expert lane + 32*i not yet selected
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = lane + 32 * i;
+            if (e < p.E) avail |= 1u << i;
+            v[i] = e < p.E ? row[e] : 0.0f;
+        }
+        int sel_e = 0;
+        float sel_v = 0.0f;
+        for (int j = 0; j < p.k; ++j) {
+            float bv = -FLT_MAX;
+            int be = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int e = lane + 32 * i;
+                if (((avail >> i) & 1u) && (be == INT_MAX || v[i] > bv || (v[i] == bv && e < be))) {
+                    bv = v[i];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+            if (lane == j) {
+                sel_e = be;
+                sel_v = bv;
+            }
+        }
+        // softmax over the k selected logits (lane j holds choice j)
+        const float zmax = __shfl_sync(0xffffffffu, sel_v, 0);
+        const float ex = lane < p.k ? expf(sel_v - zmax) : 0.0f;
+        float den = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (lane < p.k) {
+            p.idx[t * p.k + lane] = sel_e;
+            p.gate[t * p.k + lane] = ex / den;
+        }
+    }
+}
+
+template <int TX, int TM, int NT>
+cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
+{
+    constexpr int BT = (NT / TX) * TM;
+    constexpr int BE = TX * kTN;
+    constexpr size_t stage = sizeof(float) * kBK * (BT + BE);
+    constexpr size_t logits = sizeof(float) * BT * (BE + 1);
+    constexpr size_t smem = stage > logits ? stage : logits;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(route_kernel<TX, TM, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
+    route_kernel<TX, TM, NT><<<grid, NT, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
+{
+    if (a.T == 0) return cudaSuccess;
+    RouteParams p{a.x, a.wr, a.bias, a.topk_idx, a.topk_gate, a.T, a.d, a.E, a.k};
+    // every variant covers BT = 64 tokens per block and all E experts
+    if (a.E > 128) return launch_variant<32, 8, 256>(p, s);
+    if (a.E > 64) return launch_variant<16, 4, 256>(p, s);
+    if (a.E > 32) return launch_variant<8, 2, 256>(p, s);
+    if (a.E > 16) return launch_variant<4, 1, 256>(p, s);
+    if (a.E > 8) return launch_variant<2, 1, 128>(p, s);
+    return launch_variant<1, 1, 64>(p, s);
+}
+
+}  // namespace moe

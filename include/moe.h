@@ -1,0 +1,208 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300: the forward pass of one Mixture-of-Experts
+ * layer on one GB300 GPU (sm_103a), as hand-written CUDA kernels.
+ *
+ * The forward pass follows the five steps of Cui et al., "Fine-grained
+ * Computation-Communication Overlap via Tile-level Signaling and Scheduling
+ * for MoE", section 2.1: routing (top-k experts and gate weights), dispatch of
+ * each token copy to its expert, expert computation, return, and the
+ * gate-weighted sum. Each expert is the two-layer SwiGLU network of Xian et
+ * al., "X-Stage: An Overlooked Pipeline Stage for Communication-Computation
+ * Overlap in DiT Inference", section 2.2 (MegaMoE Execution): Linear-1 to the
+ * intermediate width, SwiGLU, Linear-2 back to the hidden width.
+ *
+ * Conventions shared by every entry point:
+ *   - Notation: T tokens, d hidden width, E experts, k = top_k, F = ffn
+ *     (SwiGLU intermediate width), R = T*k routed rows, S = num_segments.
+ *   - All matrices are dense row-major. bf16 is IEEE bfloat16 passed as its
+ *     16-bit pattern (moe_bf16_t); fp32 is IEEE binary32.
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise, must
+ *     be 16-byte aligned, and is owned by the caller. The library never
+ *     allocates device memory and never synchronises, except
+ *     moe_last_device_status. Work is enqueued on the caller's stream
+ *     (NULL = the legacy default stream) and returns immediately.
+ *   - Shape rules: T >= 0; d, F >= 8 and multiples of 8; 1 <= k <= 8, k <= E;
+ *     1 <= E <= 256; 1 <= S <= 64 and T % S == 0; T*k*max(d,F) < 2^40.
+ *     Violations return MOE_ERR_INVALID_ARG (bad value or pointer) or
+ *     MOE_ERR_UNSUPPORTED (legal but outside the supported range). T == 0 is
+ *     a valid empty call that enqueues nothing.
+ *   - Synchronous failures are return values. A device-side failure (a bounded
+ *     wait that ran out) is written to the status word at the start of the
+ *     workspace and read back by moe_last_device_status.
+ *   - Inputs must be finite. Calls that share a workspace must not overlap on
+ *     the GPU.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16_t;             /* raw bfloat16 bits */
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_UNSUPPORTED = 2,
+    MOE_ERR_WORKSPACE = 3,
+    MOE_ERR_CUDA = 4,
+    MOE_ERR_TIMEOUT = 5
+} moe_status_t;
+
+typedef struct {
+    int T;            /* tokens */
+    int d;            /* hidden width */
+    int E;            /* experts */
+    int top_k;        /* experts per token */
+    int ffn;          /* SwiGLU intermediate width F */
+    int num_segments; /* S owner-aligned output segments, T % S == 0 */
+} moe_shape_t;
+
+/* Tile schedule of the grouped GEMM. Both orders compute bit-identical outputs;
+ * they differ only in the order tiles run (Xian et al., section 4.2). */
+typedef enum {
+    MOE_SCHEDULE_INTERLEAVED = 0, /* Linear-2 tiles merged into the Linear-1 stream (Algorithm 1) */
+    MOE_SCHEDULE_EXPERT_WAVE = 1  /* per wave of experts: all Linear-1 tiles, then its Linear-2 tiles */
+} moe_schedule_t;
+
+typedef struct {
+    int schedule;   /* moe_schedule_t */
+    int lead_rows;  /* D: minimum lead of Linear-1 over Linear-2 in scheduler rows; 0 = default */
+    int num_ctas;   /* persistent grid size; 0 = number of SMs */
+    int l2_block_n; /* Linear-2 tile width (32..256, multiple of 32); 0 = default */
+} moe_tuning_t;
+
+/* Human-readable name of a status code. Never NULL. */
+const char *moe_status_string(moe_status_t status);
+
+/* Bytes of device workspace that moe_layer_forward needs for this shape (a
+ * superset of what moe_dispatch and moe_expert_ffn need). 0 for an invalid shape. */
+size_t moe_workspace_bytes(const moe_shape_t *shape);
+
+/* Byte offset and size of one named region inside the workspace (for
+ * inspection: routing results, the permuted rows, h, y_perm, flags).
+ * region: see MOE_WS_* below. */
+enum {
+    MOE_WS_STATUS = 0,      /* 4 x u32 device status: code, where, block, detail */
+    MOE_WS_TOPK_IDX = 1,    /* [T,k] int32 */
+    MOE_WS_TOPK_GATE = 2,   /* [T,k] fp32 */
+    MOE_WS_COUNTS = 3,      /* [E] int32 */
+    MOE_WS_OFFSETS = 4,     /* [E+1] int32 */
+    MOE_WS_ROW_OF_SLOT = 5, /* [R] int32 */
+    MOE_WS_SLOT_OF_ROW = 6, /* [R] int32 */
+    MOE_WS_X_PERM = 7,      /* [R,d] bf16 */
+    MOE_WS_H = 8,           /* [R,F] bf16: SwiGLU activations */
+    MOE_WS_Y_PERM = 9,      /* [R,d] bf16 */
+    MOE_WS_CHUNK_BASE = 10, /* dispatch scratch: [chunks,E] int32 */
+    MOE_WS_L1_DONE = 11,    /* per scheduler row: finished Linear-1 tiles, u32 */
+    MOE_WS_L2_FLAGS = 12,   /* per Linear-2 tile: ready flag = epoch of the call that wrote it, u32 */
+    MOE_WS_NUM_REGIONS = 13
+};
+moe_status_t moe_workspace_region(const moe_shape_t *shape, int region, size_t *offset,
+                                  size_t *bytes);
+
+/* Step 1, routing (Cui et al. section 2.1 step 1; Xian et al. section 2.2).
+ *   z[t,e] = sum_i x[t,i] * w_router[e,i] (+ expert_bias[e]), accumulated in
+ *   fp32 in ascending i; topk_idx[t,:] = the k largest z, descending, ties to
+ *   the lower expert index; topk_gate[t,:] = softmax of those k logits.
+ * x [T,d] bf16, w_router [E,d] bf16, expert_bias [E] fp32 or NULL,
+ * topk_idx [T,k] int32 (out), topk_gate [T,k] fp32 (out). */
+moe_status_t moe_route(const moe_shape_t *shape, const moe_bf16_t *x, const moe_bf16_t *w_router,
+                       const float *expert_bias, int32_t *topk_idx, float *topk_gate,
+                       moe_stream_t stream);
+
+/* Step 2, dispatch (Cui et al. section 2.1 step 2): a stable counting sort of
+ * the R token copies by expert, in (token, choice) order.
+ *   expert_counts[e] = #{(t,j): topk_idx[t,j] == e}; expert_offsets = exclusive
+ *   scan (E+1 entries, last = R); row_of_slot[t*k+j] = destination row;
+ *   slot_of_row = its inverse; x_perm[r] = x[slot_of_row[r] / k].
+ * x [T,d] bf16, topk_idx [T,k] int32, outputs as named; ws: at least
+ * moe_workspace_bytes(shape) bytes (uses the CHUNK_BASE and STATUS regions).
+ * An expert id outside [0,E) is skipped (its row_of_slot entry becomes -1, it
+ * is not counted) and recorded as MOE_ERR_INVALID_ARG in the device status. */
+moe_status_t moe_dispatch(const moe_shape_t *shape, const moe_bf16_t *x, const int32_t *topk_idx,
+                          int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_of_slot,
+                          int32_t *slot_of_row, moe_bf16_t *x_perm, void *ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* Step 3, expert computation (Xian et al. section 2.2) as one persistent
+ * grouped GEMM over all experts (tcgen05 MMA, bf16 in, fp32 accumulation in
+ * tensor memory):
+ *   for rows r in [off[e], off[e+1]):
+ *     h[r]      = bf16( silu(x_perm[r] W1[e]^T) * (x_perm[r] W3[e]^T) )
+ *     y_perm[r] = bf16( h[r] W2[e]^T )
+ * Linear-2 tiles are interleaved with Linear-1 tiles (Xian et al., Algorithm 1)
+ * and each publishes a ready flag after its store (Cui et al. section 3.3.1).
+ * x_perm [R,d] bf16; expert_offsets [E+1] int32 (non-decreasing, off[0]=0,
+ * off[E]=R; other offsets are recorded as MOE_ERR_INVALID_ARG in the device
+ * status and nothing is computed); W1, W3 [E,F,d] bf16; W2 [E,d,F] bf16;
+ * y_perm [R,d] bf16 (out); h lives in the workspace (region MOE_WS_H). */
+moe_status_t moe_expert_ffn(const moe_shape_t *shape, const moe_bf16_t *x_perm,
+                            const int32_t *expert_offsets, const moe_bf16_t *W1,
+                            const moe_bf16_t *W3, const moe_bf16_t *W2, moe_bf16_t *y_perm,
+                            void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_expert_ffn with an explicit tile schedule (tuning may be NULL = defaults). */
+moe_status_t moe_expert_ffn_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,
+                                  const moe_bf16_t *x_perm, const int32_t *expert_offsets,
+                                  const moe_bf16_t *W1, const moe_bf16_t *W3, const moe_bf16_t *W2,
+                                  moe_bf16_t *y_perm, void *ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* Steps 4-5, combine and weighted sum (Cui et al. section 2.1 steps 4-5):
+ *   out[t] = bf16( sum_j topk_gate[t,j] * y_perm[row_of_slot[t*k+j]] ), an fp32
+ *   sum in j order; token t is row (t mod T/S) of segment t / (T/S).
+ * y_perm [R,d] bf16, topk_gate [T,k] fp32, row_of_slot [R] int32;
+ * out_segments: HOST array of S device pointers, each [T/S, d] bf16 (out). */
+moe_status_t moe_combine(const moe_shape_t *shape, const moe_bf16_t *y_perm,
+                         const float *topk_gate, const int32_t *row_of_slot,
+                         moe_bf16_t *const *out_segments, moe_stream_t stream);
+
+/* The whole layer: route -> dispatch -> grouped SwiGLU GEMM -> combine, six
+ * kernel launches on one stream, no host synchronisation. Intermediates
+ * (routing, permutation, x_perm, h, y_perm) stay in the workspace regions. */
+moe_status_t moe_layer_forward(const moe_shape_t *shape, const moe_bf16_t *x,
+                               const moe_bf16_t *w_router, const float *expert_bias,
+                               const moe_bf16_t *W1, const moe_bf16_t *W3, const moe_bf16_t *W2,
+                               moe_bf16_t *const *out_segments, void *ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
+/* moe_layer_forward with an explicit tile schedule (tuning may be NULL). */
+moe_status_t moe_layer_forward_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,
+                                     const moe_bf16_t *x, const moe_bf16_t *w_router,
+                                     const float *expert_bias, const moe_bf16_t *W1,
+                                     const moe_bf16_t *W3, const moe_bf16_t *W2,
+                                     moe_bf16_t *const *out_segments, void *ws, size_t ws_bytes,
+                                     moe_stream_t stream);
+
+/* moe_layer_forward_tuned that also records caller-created CUDA events
+ * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries:
+ * stage_events[0] before routing, [1] after routing, [2] after dispatch,
+ * [3] after the grouped GEMM, [4] after combine. stage_events may be NULL;
+ * otherwise all five entries must be valid events of the stream's device. */
+moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *tuning,
+                                  const moe_bf16_t *x, const moe_bf16_t *w_router,
+                                  const float *expert_bias, const moe_bf16_t *W1,
+                                  const moe_bf16_t *W3, const moe_bf16_t *W2,
+                                  moe_bf16_t *const *out_segments, void *ws, size_t ws_bytes,
+                                  moe_stream_t stream, void *const *stage_events);
+
+/* Synchronises `stream`, returns the device status recorded in `ws`
+ * (MOE_OK, or MOE_ERR_TIMEOUT when a bounded wait ran out) and clears it.
+ * A failed CUDA call returns MOE_ERR_CUDA. */
+moe_status_t moe_last_device_status(void *ws, moe_stream_t stream);
+
+/* Detail words of the last device failure (valid after moe_last_device_status
+ * returned non-OK): where (kernel/role code), block index, detail. */
+void moe_last_device_detail(uint32_t *where, uint32_t *block, uint32_t *detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,129 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every entry point
+include/moe.h declares, and its host-side argument checks and workspace layout
+behave as documented. No call here reaches the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import grouped_gemm_softmax_gb300 as moe
+from grouped_gemm_softmax_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer_forward",
+                     "moe_workspace_bytes", "moe_last_device_status", "moe_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_status_strings(lib):
+    assert moe._status_string(0) == "ok"
+    assert moe._status_string(5) == "device wait timed out"
+    assert moe._status_string(99) == "unknown status"
+
+
+def test_workspace_layout_regions_are_disjoint_and_aligned(lib):
+    s = moe.Shape(T=4096, d=2048, E=64, top_k=6, ffn=1408)
+    total = moe.workspace_bytes(s)
+    R = s.R
+    expect = {moe.WS.X_PERM: R * s.d * 2, moe.WS.H: R * s.ffn * 2, moe.WS.Y_PERM: R * s.d * 2,
+              moe.WS.TOPK_IDX: R * 4, moe.WS.ROW_OF_SLOT: R * 4, moe.WS.OFFSETS: (s.E + 1) * 4}
+    spans = []
+    for r in range(13):
+        off, nb = moe.workspace_region(s, r)
+        assert off % 1024 == 0
+        assert off + nb <= total
+        spans.append((off, off + nb))
+        if r in expect:
+            assert nb == expect[r]
+    assert moe.workspace_region(s, moe.WS.STATUS)[0] == 0
+    spans.sort()
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    # h dominates: R*F*2 + 2*R*d*2 plus small regions
+    assert total < (R * s.ffn * 2 + 2 * R * s.d * 2) * 1.1
+
+
+@pytest.mark.parametrize("shape,status", [
+    (dict(T=8, d=12, E=4, top_k=2, ffn=16), 1),       # d not a multiple of 8
+    (dict(T=8, d=16, E=4, top_k=2, ffn=20), 1),       # ffn not a multiple of 8
+    (dict(T=8, d=16, E=2, top_k=3, ffn=16), 1),       # k > E
+    (dict(T=9, d=16, E=4, top_k=2, ffn=16, num_segments=2), 1),  # T % S != 0
+    (dict(T=8, d=16, E=257, top_k=2, ffn=16), 2),     # too many experts
+    (dict(T=8, d=16, E=16, top_k=9, ffn=16), 2),      # k > 8
+    (dict(T=-1, d=16, E=4, top_k=2, ffn=16), 1),
+    (dict(T=130, d=16, E=4, top_k=2, ffn=16, num_segments=65), 2),
+])
+def test_invalid_shapes_are_rejected_on_the_host(lib, shape, status):
+    s = moe.Shape(**shape)
+    assert moe.workspace_bytes(s) == 0
+    st = lib.moe_route(ctypes.byref(s.c()), None, None, None, None, None, None)
+    assert st == status
+
+
+def test_null_pointers_and_small_workspace_are_rejected_on_the_host(lib):
+    s = moe.Shape(T=64, d=64, E=4, top_k=2, ffn=64)
+    c = ctypes.byref(s.c())
+    assert lib.moe_route(c, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(c, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check fails first
+    nb = moe.workspace_bytes(s)
+    assert lib.moe_expert_ffn(c, fake, fake, fake, fake, fake, fake, fake, nb - 1, None) == \
+        moe.MOE_ERR_WORKSPACE
+    assert lib.moe_layer_forward(c, fake, fake, None, fake, fake, fake, None, fake, nb - 1, None) == \
+        moe.MOE_ERR_WORKSPACE
+    # misaligned pointer
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.moe_expert_ffn(c, mis, fake, fake, fake, fake, fake, fake, nb, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    bad_tune = moe.Tuning(schedule=7)
+    assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad_tune.c()), fake, fake, fake, fake, fake, fake,
+                                    fake, nb, None) == moe.MOE_ERR_INVALID_ARG
+    bad_tune = moe.Tuning(l2_block_n=48)
+    assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad_tune.c()), fake, fake, fake, fake, fake, fake,
+                                    fake, nb, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_call_enqueues_nothing(lib):
+    s = moe.Shape(T=0, d=64, E=4, top_k=2, ffn=64)
+    assert moe.workspace_bytes(s) > 0
+    c = ctypes.byref(s.c())
+    assert lib.moe_route(c, None, None, None, None, None, None) == moe.MOE_OK
+    assert lib.moe_combine(c, None, None, None, None, None) == moe.MOE_OK
+    fake = ctypes.c_void_p(1 << 20)
+    nb = moe.workspace_bytes(s)
+    assert lib.moe_expert_ffn(c, None, None, None, None, None, None, fake, nb, None) == moe.MOE_OK
+    assert lib.moe_layer_forward(c, None, None, None, None, None, None, None, fake, nb, None) == moe.MOE_OK
+
+
+def test_binding_rejects_wrong_tensors_before_the_library():
+    import torch
+    s = moe.Shape(T=4, d=8, E=2, top_k=1, ffn=8)
+    with pytest.raises(TypeError):
+        moe.route(s, torch.zeros(4, 8), torch.zeros(2, 8, dtype=torch.bfloat16), None,
+                  torch.zeros(4, dtype=torch.int32), torch.zeros(4))
+    with pytest.raises(ValueError):  # CPU tensors are refused: no host fallback exists
+        moe.route(s, torch.zeros(4, 8, dtype=torch.bfloat16), torch.zeros(2, 8, dtype=torch.bfloat16),
+                  None, torch.zeros(4, dtype=torch.int32), torch.zeros(4))

@@ -1,0 +1,108 @@
+"""GPU grouped SwiGLU GEMM (moe_expert_ffn) against the oracle's per-row expert
+FFN: h and y_perm within the bf16 tolerances, on ragged expert sizes (empty
+experts, one-row experts, tiles that straddle experts, K and N tails), both
+tile schedules bit-identical, and every Linear-2 tile's ready flag published."""
+import numpy as np
+import pytest
+import torch
+
+import grouped_gemm_softmax_gb300 as moe
+import oracle
+import synth
+from gpu_helpers import assert_close, bits, need_gpu, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def make_case(counts, d, F, seed=0):
+    counts = np.asarray(counts, np.int64)
+    E = len(counts)
+    R = int(counts.sum())
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = synth.gaussian_bf16((R, d), 1.0, seed, synth.TID_ROWS, "cuda")
+    w1 = synth.gaussian_bf16((E, F, d), d ** -0.5, seed, synth.TID_W1, "cuda")
+    w3 = synth.gaussian_bf16((E, F, d), d ** -0.5, seed, synth.TID_W3, "cuda")
+    w2 = synth.gaussian_bf16((E, d, F), F ** -0.5, seed, synth.TID_W2, "cuda")
+    return dict(counts=counts, offsets=offsets, x=x, w1=w1, w3=w3, w2=w2, E=E, R=R, d=d, F=F)
+
+
+def run_ffn(c, tuning=None, ws=None):
+    # the shape's T*k must equal R: use k = 1 and T = R
+    s = moe.Shape(T=c["R"], d=c["d"], E=c["E"], top_k=1, ffn=c["F"])
+    if ws is None:
+        ws = moe.alloc_workspace(s)
+    y = torch.full((c["R"], c["d"]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    off = torch.from_numpy(c["offsets"]).cuda()
+    moe.expert_ffn(s, c["x"], off, c["w1"], c["w3"], c["w2"], y, ws, tuning=tuning)
+    st = moe.last_device_status(ws)
+    assert st == moe.MOE_OK, (st, moe.last_device_detail())
+    h = moe.ws_view(ws, s, moe.WS.H, torch.bfloat16, (c["R"], c["F"])).clone()
+    return s, ws, h, y
+
+
+def oracle_rows(c, rows):
+    er = np.repeat(np.arange(c["E"]), c["counts"]).astype(np.int32)[rows]
+    return oracle.ffn_rows(bits(c["x"])[rows], er, bits(c["w1"]), bits(c["w3"]), bits(c["w2"]), c["E"],
+                           keep_h=True)
+
+
+CASES = {
+    "single_expert_one_tile": ([128], 256, 256),
+    "single_expert_ragged": ([300], 256, 512),
+    "tiny_like": ([70, 0, 129, 1, 255, 57, 0, 0], 256, 512),
+    "k_and_n_tails": ([200, 33, 140], 136, 200),
+    "wide_d_tail": ([260, 70], 1160, 128),
+    "dit_like_d": ([130, 5, 400], 1152, 384),
+    "many_small_experts": ([3, 1, 0, 7, 130, 2, 0, 64] * 8, 128, 256),
+    "one_row": ([1], 64, 64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_ffn_parity(name):
+    need_gpu()
+    counts, d, F = CASES[name]
+    c = make_case(counts, d, F, seed=len(name))
+    _, _, h, y = run_ffn(c)
+    rows = np.arange(c["R"])
+    href, yref = oracle_rows(c, rows)
+    assert_close(to_f64(h), href, f"{name} h")
+    assert_close(to_f64(y), yref, f"{name} y")
+
+
+def test_ffn_schedules_and_grids_are_bit_identical():
+    need_gpu()
+    c = make_case([70, 0, 129, 1, 255, 57, 300, 12] * 4, 256, 384, seed=9)
+    _, _, h0, y0 = run_ffn(c)
+    variants = [moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE), moe.Tuning(lead_rows=1),
+                moe.Tuning(lead_rows=50), moe.Tuning(num_ctas=1), moe.Tuning(num_ctas=7),
+                moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE, num_ctas=3)]
+    for t in variants:
+        _, _, h, y = run_ffn(c, tuning=t)
+        assert torch.equal(h.view(torch.int16), h0.view(torch.int16)), t
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16)), t
+
+
+@pytest.mark.parametrize("n2", [64, 128, 192, 256])
+def test_ffn_l2_tile_widths(n2):
+    need_gpu()
+    c = make_case([150, 90], 384, 256, seed=n2)
+    _, _, h, y = run_ffn(c, tuning=moe.Tuning(l2_block_n=n2))
+    href, yref = oracle_rows(c, np.arange(c["R"]))
+    assert_close(to_f64(y), yref, f"N2={n2} y")
+
+
+def test_ready_flags_carry_the_call_epoch():
+    need_gpu()
+    counts = [70, 0, 129, 1, 255]
+    c = make_case(counts, 256, 256, seed=4)
+    s, ws, _, _ = run_ffn(c)
+    rows = int(sum((n + 127) // 128 for n in counts))
+    p2 = 1  # d = 256 -> one 256-wide Linear-2 tile per row
+    flags = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (rows * p2,)).cpu().numpy()
+    assert flags[0] != 0 and np.all(flags == flags[0])
+    done = moe.ws_view(ws, s, moe.WS.L1_DONE, torch.int32, (rows,)).cpu().numpy()
+    assert np.all(done == 2)  # F = 256 -> two Linear-1 tiles per row
+    run_ffn(c, ws=ws)
+    flags2 = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (rows * p2,)).cpu().numpy()
+    assert np.all(flags2 == flags2[0]) and flags2[0] != flags[0]

@@ -1,0 +1,118 @@
+"""The fused layer (moe_layer_forward) end to end against the oracle.
+
+Small cases compare every output. The full-size workloads (the bench's
+configuration among them, in the launch configuration the bench times)
+compare routing for every token bit-exactly, the dispatch permutation
+bit-exactly, y_perm on a seeded sample of rows and the layer output on a
+seeded sample of tokens within the stated tolerances."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import grouped_gemm_softmax_gb300 as moe
+import oracle
+import synth
+from conftest import f32_to_bf16_bits
+from gpu_helpers import (GpuLayer, assert_close, bits, check_dispatch, check_route, compact_experts,
+                         custom_cfg, need_gpu, oracle_route, sample_tokens, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def test_hand_example_on_gpu():
+    """The hand-worked example, zero-padded to d = F = 8 (padding changes no output)."""
+    need_gpu()
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_example.json")))
+    T, E, k, d, F = 4, 3, 2, 8, 8
+    x = np.zeros((T, d)); x[:, :2] = g["x"]
+    wr = np.zeros((E, d)); wr[:, :2] = g["w_router"]
+    w1 = np.zeros((E, F, d)); w1[:, :1, :2] = g["W1"]
+    w3 = np.zeros((E, F, d)); w3[:, :1, :2] = g["W3"]
+    w2 = np.zeros((E, d, F)); w2[:, :2, :1] = g["W2"]
+    dev = lambda a: synth.bits_to_bf16(f32_to_bf16_bits(a)).cuda()
+    s = moe.Shape(T=T, d=d, E=E, top_k=k, ffn=F)
+    ws = moe.alloc_workspace(s)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    moe.layer_forward(s, dev(x), dev(wr), None, dev(w1), dev(w3), dev(w2), [out], ws)
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    got = to_f64(out)
+    np.testing.assert_array_equal(got[:, 2:], 0.0)
+    # h and y are rounded to bf16 on the GPU: a few bf16 ulps of the closed forms
+    np.testing.assert_allclose(got[:, :2], np.array(g["out"]), rtol=2e-2, atol=1e-3)
+    idx = moe.ws_view(ws, s, moe.WS.TOPK_IDX, torch.int32, (T, k)).cpu().numpy()
+    np.testing.assert_array_equal(idx, g["topk_idx"])
+    sor = moe.ws_view(ws, s, moe.WS.SLOT_OF_ROW, torch.int32, (T * k,)).cpu().numpy()
+    np.testing.assert_array_equal(sor, g["slot_of_row"])
+
+
+def _full_compare(layer, out, n_tokens, n_rows, seed=0):
+    cfg = layer.cfg
+    ref = oracle_route(layer)
+    idx, gate = layer.routing()
+    check_route(idx, gate, ref)
+    disp = check_dispatch(layer.dispatch_state(), ref.idx, cfg.E)
+    # y_perm on sampled rows (first and last row of every expert among them)
+    rows = set()
+    rng = np.random.default_rng(seed)
+    for e in rng.choice(cfg.E, size=min(cfg.E, 8), replace=False):
+        a, b = disp.offsets[e], disp.offsets[e + 1]
+        if b > a:
+            rows.update([a, b - 1, (a + b) // 2])
+    rows.update(rng.choice(cfg.R, size=min(cfg.R, n_rows), replace=False).tolist())
+    rows = np.array(sorted(rows), np.int64)
+    er = np.searchsorted(disp.offsets, rows, side="right") - 1
+    tokens = sample_tokens(cfg.T, n_tokens, seed)
+    used = set(er.tolist()) | set(ref.idx[tokens].reshape(-1).tolist())
+    w1, w3, w2, remap = compact_experts(layer, used)
+    xb = bits(layer.inp.x)
+    _, yref = oracle.ffn_rows(xb[disp.slot_of_row[rows] // cfg.k], remap[er], w1, w3, w2, len(remap))
+    yperm = moe.ws_view(layer.ws, layer.shape, moe.WS.Y_PERM, torch.bfloat16, (cfg.R, cfg.d))
+    assert_close(to_f64(yperm[torch.from_numpy(rows).cuda()]), yref, f"{cfg.name} y_perm rows")
+    oref = oracle.layer_tokens(xb, remap[ref.idx], ref.gate, w1, w3, w2, tokens, len(remap))
+    return assert_close(to_f64(out[torch.from_numpy(tokens.astype(np.int64)).cuda()]), oref,
+                        f"{cfg.name} out")
+
+
+def test_tiny_layer_every_token():
+    need_gpu()
+    layer = GpuLayer(synth.CONFIGS["tiny"])
+    out = layer.forward()
+    _full_compare(layer, out, n_tokens=256, n_rows=512)
+
+
+@pytest.mark.parametrize("cfg", [custom_cfg(1000, 136, 5, 3, 200, S=8, zipf_s=2.0),
+                                 custom_cfg(333, 256, 33, 4, 128, S=3, zipf_s=1.0),
+                                 custom_cfg(64, 512, 256, 8, 64),
+                                 custom_cfg(1, 64, 4, 2, 64)], ids=lambda c: f"T{c.T}_E{c.E}")
+def test_ragged_layers_every_token(cfg):
+    need_gpu()
+    layer = GpuLayer(cfg, seed=1)
+    out = layer.forward()
+    _full_compare(layer, out, n_tokens=cfg.T, n_rows=cfg.R)
+
+
+def test_schedules_and_repeat_calls_are_bit_identical():
+    need_gpu()
+    layer = GpuLayer(synth.CONFIGS["tiny"])
+    a = layer.forward().clone()
+    b = layer.forward(tuning=moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE)).clone()
+    c = layer.forward().clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mid", "dit", "fine", "coarse"])
+def test_full_size_configs(name):
+    need_gpu()
+    layer = GpuLayer(synth.CONFIGS[name])
+    out = layer.forward()
+    out2 = layer.forward(tuning=moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE))
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    maxrel, fro = _full_compare(layer, out, n_tokens=24, n_rows=48)
+    print(f"{name}: max err / max|ref| = {maxrel:.2e}, rel Frobenius = {fro:.2e}")
+    del layer
+    torch.cuda.empty_cache()
