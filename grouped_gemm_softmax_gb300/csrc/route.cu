@@ -14,8 +14,9 @@
 // selection is therefore reproducible bit for bit by any implementation of
 // that sum.
 //
-// Block tile: BT = 64 tokens x BE = 8*TX experts, staged through shared memory
-// 32 features at a time (fp32, transposed), each thread owning TM tokens x 8
+// Block tile: BT tokens x BE >= E experts, staged through shared memory 32
+// features at a time (fp32, transposed; the next chunk is prefetched into
+// registers while the current one is used), each thread owning TM tokens x TN
 // experts. Then one warp per token runs k rounds of a shuffle arg-max over the
 // block's logits and writes idx and gates.
 #include <cuda_bf16.h>
@@ -26,8 +27,7 @@
 namespace moe {
 namespace {
 
-constexpr int kBK = 32;
-constexpr int kTN = 8;
+constexpr int kBK = 32;  // features per shared-memory chunk
 
 struct RouteParams {
     const uint16_t *x;
@@ -43,13 +43,17 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
     return __uint_as_float(bits16 << 16);
 }
 
-template <int TX, int TM, int NT>
+template <int TX, int TM, int TN, int NT>
 __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
 {
     constexpr int TY = NT / TX;
-    constexpr int BT = TY * TM;
-    constexpr int BE = TX * kTN;
+    constexpr int BT = TY * TM;   // tokens per block
+    constexpr int BE = TX * TN;   // experts per block (>= E)
     constexpr int NW = NT / 32;
+    constexpr int XV = BT * (kBK / 8);  // 16-byte vectors of x per chunk
+    constexpr int WV = BE * (kBK / 8);  // 16-byte vectors of Wr per chunk
+    constexpr int XPT = (XV + NT - 1) / NT;
+    constexpr int WPT = (WV + NT - 1) / NT;
     extern __shared__ float rsm[];
     float *xs = rsm;             // [kBK][BT]
     float *ws = rsm + kBK * BT;  // [kBK][BE]
@@ -60,53 +64,83 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
     const int ty = tid / TX;
     const long t0 = static_cast<long>(blockIdx.x) * BT;
 
-    float acc[TM][kTN];
+    float acc[TM][TN];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < kTN; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
-    // staging: 16-byte vectors (8 features) of BT token rows and BE expert rows
-    constexpr int XV = BT * (kBK / 8);
-    constexpr int WV = BE * (kBK / 8);
+    // register prefetch of the next chunk (global -> registers -> shared)
+    uint4 px[XPT], pw[WPT];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int u = 0; u < XPT; ++u) {
+            const int v = tid + u * NT;
+            px[u] = make_uint4(0, 0, 0, 0);
+            if (v < XV) {
+                const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
+                const long t = t0 + r;
+                if (t < p.T && k0 + c8 < p.d)
+                    px[u] = __ldg(reinterpret_cast<const uint4 *>(p.x + t * p.d + k0 + c8));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < WPT; ++u) {
+            const int v = tid + u * NT;
+            pw[u] = make_uint4(0, 0, 0, 0);
+            if (v < WV) {
+                const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
+                if (r < p.E && k0 + c8 < p.d)
+                    pw[u] = __ldg(reinterpret_cast<const uint4 *>(p.wr + static_cast<long>(r) * p.d +
+                                                                  k0 + c8));
+            }
+        }
+    };
+    auto stage = [&]() {
+#pragma unroll
+        for (int u = 0; u < XPT; ++u) {
+            const int v = tid + u * NT;
+            if (v < XV) {
+                const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
+                const uint32_t w[4] = {px[u].x, px[u].y, px[u].z, px[u].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    xs[(c8 + 2 * h) * BT + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
+                    xs[(c8 + 2 * h + 1) * BT + r] = bf16_bits_to_f32(w[h] >> 16);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < WPT; ++u) {
+            const int v = tid + u * NT;
+            if (v < WV) {
+                const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
+                const uint32_t w[4] = {pw[u].x, pw[u].y, pw[u].z, pw[u].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    ws[(c8 + 2 * h) * BE + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
+                    ws[(c8 + 2 * h + 1) * BE + r] = bf16_bits_to_f32(w[h] >> 16);
+                }
+            }
+        }
+    };
+
+    fetch(0);
     for (int k0 = 0; k0 < p.d; k0 += kBK) {
-        for (int v = tid; v < XV; v += NT) {
-            const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
-            const long t = t0 + r;
-            uint4 q = make_uint4(0, 0, 0, 0);
-            if (t < p.T && k0 + c8 < p.d)
-                q = *reinterpret_cast<const uint4 *>(p.x + t * p.d + k0 + c8);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                xs[(c8 + 2 * h) * BT + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
-                xs[(c8 + 2 * h + 1) * BT + r] = bf16_bits_to_f32(w[h] >> 16);
-            }
-        }
-        for (int v = tid; v < WV; v += NT) {
-            const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
-            uint4 q = make_uint4(0, 0, 0, 0);
-            if (r < p.E && k0 + c8 < p.d)
-                q = *reinterpret_cast<const uint4 *>(p.wr + static_cast<long>(r) * p.d + k0 + c8);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                ws[(c8 + 2 * h) * BE + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
-                ws[(c8 + 2 * h + 1) * BE + r] = bf16_bits_to_f32(w[h] >> 16);
-            }
-        }
+        stage();
         __syncthreads();
-#pragma unroll 4
+        if (k0 + kBK < p.d) fetch(k0 + kBK);
+#pragma unroll 8
         for (int kk = 0; kk < kBK; ++kk) {
-            float xv[TM], wv[kTN];
+            float xv[TM], wv[TN];
 #pragma unroll
             for (int i = 0; i < TM; ++i) xv[i] = xs[kk * BT + ty * TM + i];
 #pragma unroll
-            for (int j = 0; j < kTN; ++j) wv[j] = ws[kk * BE + tx * kTN + j];
+            for (int j = 0; j < TN; ++j) wv[j] = ws[kk * BE + tx * TN + j];
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < kTN; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
         }
         __syncthreads();
     }
@@ -115,8 +149,8 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
 #pragma unroll
-        for (int j = 0; j < kTN; ++j) {
-            const int e = tx * kTN + j;
+        for (int j = 0; j < TN; ++j) {
+            const int e = tx * TN + j;
             float z = acc[i][j];
             if (p.bias != nullptr && e < p.E) z = z + p.bias[e];
             lg[(ty * TM + i) * (BE + 1) + e] = z;
@@ -179,24 +213,24 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
     }
 }
 
-template <int TX, int TM, int NT>
+template <int TX, int TM, int TN, int NT>
 cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
 {
     constexpr int BT = (NT / TX) * TM;
-    constexpr int BE = TX * kTN;
+    constexpr int BE = TX * TN;
     constexpr size_t stage = sizeof(float) * kBK * (BT + BE);
     constexpr size_t logits = sizeof(float) * BT * (BE + 1);
     constexpr size_t smem = stage > logits ? stage : logits;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel<TX, TM, NT>,
+        cudaError_t e = cudaFuncSetAttribute(route_kernel<TX, TM, TN, NT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
-    route_kernel<TX, TM, NT><<<grid, NT, smem, s>>>(p);
+    route_kernel<TX, TM, TN, NT><<<grid, NT, smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -206,13 +240,14 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
 {
     if (a.T == 0) return cudaSuccess;
     RouteParams p{a.x, a.wr, a.bias, a.topk_idx, a.topk_gate, a.T, a.d, a.E, a.k};
-    // every variant covers BT = 64 tokens per block and all E experts
-    if (a.E > 128) return launch_variant<32, 8, 256>(p, s);
-    if (a.E > 64) return launch_variant<16, 4, 256>(p, s);
-    if (a.E > 32) return launch_variant<8, 2, 256>(p, s);
-    if (a.E > 16) return launch_variant<4, 1, 256>(p, s);
-    if (a.E > 8) return launch_variant<2, 1, 128>(p, s);
-    return launch_variant<1, 1, 64>(p, s);
+    // thread tile TM tokens x TN experts; a block covers every expert and
+    // 32 tokens (64 when E > 128), so even small T gives a few blocks per SM
+    if (a.E > 128) return launch_variant<32, 8, 8, 256>(p, s);
+    if (a.E > 64) return launch_variant<32, 4, 4, 256>(p, s);
+    if (a.E > 32) return launch_variant<16, 2, 4, 256>(p, s);
+    if (a.E > 16) return launch_variant<16, 2, 2, 256>(p, s);
+    if (a.E > 8) return launch_variant<16, 2, 1, 256>(p, s);
+    return launch_variant<8, 1, 1, 256>(p, s);
 }
 
 }  // namespace moe
