@@ -52,7 +52,8 @@ class _CShape(ctypes.Structure):
 
 class _CTuning(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int), ("lead_rows", ctypes.c_int), ("num_ctas", ctypes.c_int),
-                ("l2_block_n", ctypes.c_int)]
+                ("l2_block_n", ctypes.c_int), ("group_rows", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("trace", ctypes.c_void_p)]
 
 
 @dataclass(frozen=True)
@@ -72,15 +73,25 @@ class Shape:
         return _CShape(self.T, self.d, self.E, self.top_k, self.ffn, self.num_segments)
 
 
+TRACE_WORDS = 16  # per-CTA uint64 counters written when Tuning.trace is given
+TRACE_FIELDS = ("prod_wait_empty", "prod_wait_rows", "prod_cycles", "mma_wait_full", "mma_wait_tmem",
+                "mma_cycles", "epi_wait_full", "epi_work", "epi_wait_stores", "epi_cycles", "l1_tiles",
+                "l2_tiles", "t_start_ns", "t_end_ns", "unused14", "unused15")
+
+
 @dataclass(frozen=True)
 class Tuning:
     schedule: int = SCHEDULE_INTERLEAVED
     lead_rows: int = 0
     num_ctas: int = 0
     l2_block_n: int = 0
+    group_rows: int = 0
+    trace: object = None  # optional torch int64 CUDA tensor of >= num_ctas * TRACE_WORDS entries
 
     def c(self) -> _CTuning:
-        return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n)
+        tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
+        return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
+                        0, tr)
 
 
 _lib = None

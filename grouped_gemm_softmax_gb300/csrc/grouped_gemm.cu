@@ -46,10 +46,12 @@ constexpr int kStages = 4;
 constexpr int kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
 constexpr int kBTileBytes = 256 * kBlockK * 2;      // 32 KiB
 constexpr int kL1StageBytes = kATileBytes + kBTileBytes;
+constexpr int kDefaultGroupRows = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
+constexpr int kTraceWords = 16;  // per-CTA counters when tracing is on
 
 struct GemmParams {
     const int32_t *offsets;
@@ -61,8 +63,9 @@ struct GemmParams {
     int E, d, F, R;
     int P1, P2, N2;
     int kb1, kb2;
-    int schedule, lead;
+    int schedule, lead, group;
     unsigned epoch;
+    unsigned long long *trace;
 };
 
 struct SmemCtl {
@@ -79,81 +82,16 @@ struct SmemCtl {
     long wave_tile[kMaxExperts + 1]; // first global tile index of wave w
 };
 
+// epilogue transpose buffer: per epilogue warp, 32 rows x 64 bf16 (128 B a row)
+constexpr int kEpiStageBytes = 32 * 128;
+constexpr size_t kCtlBytes = (sizeof(SmemCtl) + 127) / 128 * 128;
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * (kATileBytes + kBTileBytes) +
-                              sizeof(SmemCtl);
+                              kCtlBytes + 4 * kEpiStageBytes;
 
 struct Tile {
     int kind;  // 0 = Linear-1, 1 = Linear-2, -1 = no more tiles
     int row;
     int n;
-};
-
-// Every role of a CTA runs its own copy of this deterministic walk, so they all
-// see the same tile sequence without communicating.
-struct Scheduler {
-    long k1, k2, tot1, tot2;
-    long gi;
-    int w;
-    int P1, P2, G, D, mode;
-
-    __device__ Scheduler(const SmemCtl &c, const GemmParams &p)
-    {
-        const long P = c.row_start[p.E];
-        P1 = p.P1;
-        P2 = p.P2;
-        G = gridDim.x;
-        D = p.lead;
-        mode = p.schedule;
-        k1 = k2 = blockIdx.x;
-        tot1 = P * P1;
-        tot2 = P * P2;
-        gi = blockIdx.x;
-        w = 0;
-    }
-
-    __device__ Tile next(const SmemCtl &c)
-    {
-        Tile t;
-        if (mode == 0) {
-            if (k1 >= tot1 && k2 >= tot2) {
-                t.kind = -1;
-                return t;
-            }
-            const long p1 = (k1 < tot1) ? k1 / P1 : LONG_MAX / 2;
-            if (k2 < tot2 && k2 / P2 + D <= p1) {
-                t.kind = 1;
-                t.row = static_cast<int>(k2 / P2);
-                t.n = static_cast<int>(k2 % P2);
-                k2 += G;
-            } else {
-                t.kind = 0;
-                t.row = static_cast<int>(k1 / P1);
-                t.n = static_cast<int>(k1 % P1);
-                k1 += G;
-            }
-            return t;
-        }
-        if (gi >= c.wave_tile[c.nwaves]) {
-            t.kind = -1;
-            return t;
-        }
-        while (gi >= c.wave_tile[w + 1]) ++w;
-        long j = gi - c.wave_tile[w];
-        const int r0 = c.wave_row[w];
-        const long nr = c.wave_row[w + 1] - r0;
-        if (j < nr * P1) {
-            t.kind = 0;
-            t.row = r0 + static_cast<int>(j / P1);
-            t.n = static_cast<int>(j % P1);
-        } else {
-            j -= nr * P1;
-            t.kind = 1;
-            t.row = r0 + static_cast<int>(j / P2);
-            t.n = static_cast<int>(j % P2);
-        }
-        gi += G;
-        return t;
-    }
 };
 
 // expert owning scheduler row `row` (the last e with row_start[e] <= row)
@@ -167,6 +105,88 @@ __device__ __forceinline__ int row_expert(const SmemCtl &c, int E, int row)
     }
     return lo;
 }
+
+// Position k of a tile stream (Pn N-tiles per scheduler row) -> (row, n). Tiles
+// of one expert occupy positions [row_start[e]*Pn, row_start[e+1]*Pn); inside
+// the expert they run over groups of GM consecutive rows, N-tile-major within a
+// group, so a weight tile is reused by the group's M-tiles back to back. Every
+// tile of row p sits below position (p + GM) * Pn.
+__device__ __forceinline__ Tile stream_tile(const SmemCtl &c, int E, long k, int Pn, int GM, int kind)
+{
+    Tile t;
+    t.kind = kind;
+    const int e = row_expert(c, E, static_cast<int>(k / Pn));
+    const int r0 = c.row_start[e];
+    const long local = k - static_cast<long>(r0) * Pn;
+    const long per_group = static_cast<long>(GM) * Pn;
+    const int j = static_cast<int>(local / per_group);
+    const int gs = min(GM, c.row_start[e + 1] - r0 - j * GM);
+    const int i = static_cast<int>(local - j * per_group);
+    t.n = i / gs;
+    t.row = r0 + j * GM + i % gs;
+    return t;
+}
+
+// Every role of a CTA runs its own copy of this deterministic walk, so they all
+// see the same tile sequence without communicating.
+struct Scheduler {
+    long k1, k2, tot1, tot2;
+    long gi;
+    int w;
+    int P1, P2, G, D, GM, mode;
+
+    __device__ Scheduler(const SmemCtl &c, const GemmParams &p)
+    {
+        const long P = c.row_start[p.E];
+        P1 = p.P1;
+        P2 = p.P2;
+        G = gridDim.x;
+        D = p.lead;
+        GM = p.group;
+        mode = p.schedule;
+        k1 = k2 = blockIdx.x;
+        tot1 = P * P1;
+        tot2 = P * P2;
+        gi = blockIdx.x;
+        w = 0;
+    }
+
+    __device__ Tile next(const SmemCtl &c, int E)
+    {
+        Tile t;
+        if (mode == 0) {
+            // Algorithm 1: the Linear-1 cursor sits at row floor(k1 / P1); a
+            // Linear-2 tile goes out once its row trails that by D >= GM rows.
+            if (k1 >= tot1 && k2 >= tot2) {
+                t.kind = -1;
+                return t;
+            }
+            const long p1 = (k1 < tot1) ? k1 / P1 : LONG_MAX / 2;
+            if (k2 < tot2) {
+                const Tile t2 = stream_tile(c, E, k2, P2, GM, 1);
+                if (t2.row + D <= p1) {
+                    k2 += G;
+                    return t2;
+                }
+            }
+            t = stream_tile(c, E, k1, P1, GM, 0);
+            k1 += G;
+            return t;
+        }
+        // expert waves: all Linear-1 tiles of a wave, then its Linear-2 tiles
+        if (gi >= c.wave_tile[c.nwaves]) {
+            t.kind = -1;
+            return t;
+        }
+        while (gi >= c.wave_tile[w + 1]) ++w;
+        const long j = gi - c.wave_tile[w];
+        const int r0 = c.wave_row[w];
+        const long nr = c.wave_row[w + 1] - r0;
+        gi += G;
+        if (j < nr * P1) return stream_tile(c, E, static_cast<long>(r0) * P1 + j, P1, GM, 0);
+        return stream_tile(c, E, static_cast<long>(r0) * P2 + (j - nr * P1), P2, GM, 1);
+    }
+};
 
 __device__ __forceinline__ bool wait_rows_ready(const unsigned *ctr, unsigned target,
                                                 volatile int *cta_abort, unsigned *status,
@@ -202,7 +222,7 @@ __device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits)
 {
     const float g = __uint_as_float(g_bits);
     const float u = __uint_as_float(u_bits);
-    return g / (1.0f + __expf(-g)) * u;
+    return g * __fdividef(1.0f, 1.0f + __expf(-g)) * u;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -217,6 +237,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     uint8_t *sA = reinterpret_cast<uint8_t *>(base);
     uint8_t *sB = sA + kStages * kATileBytes;
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(sB + kStages * kBTileBytes);
+    uint8_t *s_epi = sB + kStages * kBTileBytes + kCtlBytes;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -310,6 +331,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     tc_fence_after();
     const uint32_t tmem_base = c.tmem_base;
     volatile int *abort_flag = &c.abort;
+    const bool tr = p.trace != nullptr;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -318,26 +340,31 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
+            unsigned long long w_empty = 0, w_rows = 0, t0 = tr ? clock64() : 0;
             while (ok) {
-                const Tile t = sch.next(c);
+                const Tile t = sch.next(c, E);
                 if (t.kind < 0) break;
                 const int e = row_expert(c, E, t.row);
                 const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kBlockM;
                 if (t.kind == 1) {
+                    const unsigned long long tw = tr ? clock64() : 0;
                     if (!wait_rows_ready(&p.l1_done[t.row], static_cast<unsigned>(p.P1), abort_flag,
                                          p.status, static_cast<unsigned>(t.row)))
                         break;
+                    if (tr) w_rows += clock64() - tw;
                     fence_proxy_async_global();
                 }
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
                 const uint32_t bytes =
                     t.kind == 0 ? kL1StageBytes : kATileBytes + p.N2 * kBlockK * 2;
                 for (int kb = 0; kb < nkb; ++kb) {
+                    const unsigned long long tw = tr ? clock64() : 0;
                     if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag, p.status, kWhereProducerEmpty,
                                    static_cast<unsigned>(s))) {
                         ok = false;
                         break;
                     }
+                    if (tr) w_empty += clock64() - tw;
                     mbar_arrive_expect_tx(&c.full[s], bytes);
                     uint8_t *a = sA + s * kATileBytes;
                     uint8_t *b = sB + s * kBTileBytes;
@@ -356,6 +383,12 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                     }
                 }
             }
+            if (tr) {
+                unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
+                o[0] = w_empty;
+                o[1] = w_rows;
+                o[2] = clock64() - t0;
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -366,24 +399,29 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             const uint32_t idesc1 = idesc_bf16_f32(kBlockM, 2 * kL1N);
             const uint32_t idesc2 = idesc_bf16_f32(kBlockM, p.N2);
             bool ok = true;
+            unsigned long long w_full = 0, w_tmem = 0, t0 = tr ? clock64() : 0;
             for (int tl = 0; ok; ++tl) {
-                const Tile t = sch.next(c);
+                const Tile t = sch.next(c, E);
                 if (t.kind < 0) break;
                 const int b = tl & 1;
                 const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
+                unsigned long long tw = tr ? clock64() : 0;
                 if (!mbar_wait(&c.tempty[b], aph ^ 1u, abort_flag, p.status, kWhereMmaTmemEmpty,
                                static_cast<unsigned>(tl)))
                     break;
+                if (tr) w_tmem += clock64() - tw;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b) * kAccCols;
                 const uint32_t idesc = t.kind == 0 ? idesc1 : idesc2;
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
                 for (int kb = 0; kb < nkb; ++kb) {
+                    tw = tr ? clock64() : 0;
                     if (!mbar_wait(&c.full[s], ph, abort_flag, p.status, kWhereMmaFull,
                                    static_cast<unsigned>(s))) {
                         ok = false;
                         break;
                     }
+                    if (tr) w_full += clock64() - tw;
                     tc_fence_after();
                     const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + s * kATileBytes));
                     const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + s * kBTileBytes));
@@ -401,88 +439,102 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 }
                 if (ok) mma_commit(&c.tfull[b]);
             }
+            if (tr) {
+                unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
+                o[3] = w_full;
+                o[4] = w_tmem;
+                o[5] = clock64() - t0;
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;
-        const int r_in_tile = q * 32 + lane;
+        const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         const bool publisher = (warp == 2 && lane == 0);
         Scheduler sch(c, p);
+        unsigned long long w_full = 0, w_work = 0, w_stores = 0, n1 = 0, n2 = 0;
+        const unsigned long long t0 = tr ? clock64() : 0;
+        if (tr && publisher) p.trace[blockIdx.x * kTraceWords + 12] = globaltimer_ns();
         for (int tl = 0;; ++tl) {
-            const Tile t = sch.next(c);
+            const Tile t = sch.next(c, E);
             if (t.kind < 0) break;
             const int b = tl & 1;
             const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
+            unsigned long long tw = tr ? clock64() : 0;
             if (!mbar_wait(&c.tfull[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
                            static_cast<unsigned>(tl)))
                 break;
+            if (tr) {
+                const unsigned long long now = clock64();
+                w_full += now - tw;
+                tw = now;
+                if (t.kind == 0) ++n1;
+                else ++n2;
+            }
             tc_fence_after();
             const int e = row_expert(c, E, t.row);
             const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kBlockM;
             const int valid_rows = min(kBlockM, c.offs[e + 1] - row0);
-            const bool valid = r_in_tile < valid_rows;
-            const long grow = static_cast<long>(row0) + r_in_tile;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(b) * kAccCols;
-            if (t.kind == 0) {
-                for (int c32 = 0; c32 < kL1N / 32; ++c32) {
-                    uint32_t g[32], u[32];
-                    tmem_load_32cols(tbase + c32 * 32, g);
-                    tmem_load_32cols(tbase + kL1N + c32 * 32, u);
-                    const int col0 = t.n * kL1N + c32 * 32;
-                    if (valid) {
-                        uint16_t *dst = p.h + grow * p.F + col0;
+            // 64 columns at a time: tensor memory -> registers (thread = row) ->
+            // swizzled shared-memory transpose -> 16-byte stores that cover four
+            // full 128-byte row segments per warp instruction.
+            uint8_t *stg = s_epi + (warp - 2) * kEpiStageBytes;
+            const int nchunks = t.kind == 0 ? kL1N / 64 : p.N2 / 64;
+            uint16_t *const out_base = t.kind == 0 ? p.h : p.y;
+            const int out_ld = t.kind == 0 ? p.F : p.d;
+            const int col_base = t.kind == 0 ? t.n * kL1N : t.n * p.N2;
+            for (int ch = 0; ch < nchunks; ++ch) {
+                uint32_t pk[32];
+                if (t.kind == 0) {
+                    uint32_t g[64], u[64];
+                    tmem_load_2x64cols(tbase + ch * 64, tbase + kL1N + ch * 64, g, u);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            if (col0 + v * 8 < p.F) {
-                                uint4 pk;
-                                pk.x = pack_bf16x2(silu_mul(g[v * 8 + 0], u[v * 8 + 0]),
-                                                   silu_mul(g[v * 8 + 1], u[v * 8 + 1]));
-                                pk.y = pack_bf16x2(silu_mul(g[v * 8 + 2], u[v * 8 + 2]),
-                                                   silu_mul(g[v * 8 + 3], u[v * 8 + 3]));
-                                pk.z = pack_bf16x2(silu_mul(g[v * 8 + 4], u[v * 8 + 4]),
-                                                   silu_mul(g[v * 8 + 5], u[v * 8 + 5]));
-                                pk.w = pack_bf16x2(silu_mul(g[v * 8 + 6], u[v * 8 + 6]),
-                                                   silu_mul(g[v * 8 + 7], u[v * 8 + 7]));
-                                *reinterpret_cast<uint4 *>(dst + v * 8) = pk;
-                            }
-                        }
-                    }
-                }
-            } else {
-                const int nchunks = p.N2 / 32;
-                for (int c32 = 0; c32 < nchunks; ++c32) {
-                    uint32_t a[32];
-                    tmem_load_32cols(tbase + c32 * 32, a);
-                    const int col0 = t.n * p.N2 + c32 * 32;
-                    if (valid) {
-                        uint16_t *dst = p.y + grow * p.d + col0;
+                    for (int i = 0; i < 32; ++i)
+                        pk[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]),
+                                            silu_mul(g[2 * i + 1], u[2 * i + 1]));
+                } else {
+                    uint32_t a[64];
+                    tmem_load_64cols(tbase + ch * 64, a);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            if (col0 + v * 8 < p.d) {
-                                uint4 pk;
-                                pk.x = pack_bf16x2(__uint_as_float(a[v * 8 + 0]),
-                                                   __uint_as_float(a[v * 8 + 1]));
-                                pk.y = pack_bf16x2(__uint_as_float(a[v * 8 + 2]),
-                                                   __uint_as_float(a[v * 8 + 3]));
-                                pk.z = pack_bf16x2(__uint_as_float(a[v * 8 + 4]),
-                                                   __uint_as_float(a[v * 8 + 5]));
-                                pk.w = pack_bf16x2(__uint_as_float(a[v * 8 + 6]),
-                                                   __uint_as_float(a[v * 8 + 7]));
-                                *reinterpret_cast<uint4 *>(dst + v * 8) = pk;
-                            }
-                        }
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
                 }
+                // row `lane` of the warp's 32-row slab: 8 pieces of 16 B, piece j at
+                // slot j ^ (lane & 7) (conflict-free writes and reads)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                __syncwarp();
+                const int piece = lane & 7;
+                const int col = col_base + ch * 64 + piece * 8;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = i * 4 + (lane >> 3);  // row within the warp's slab
+                    const uint4 v =
+                        *reinterpret_cast<const uint4 *>(stg + r * 128 + ((piece ^ (r & 7)) << 4));
+                    if (q * 32 + r < valid_rows && col < out_ld)
+                        *reinterpret_cast<uint4 *>(out_base + (static_cast<long>(row0) + q * 32 + r) *
+                                                                  out_ld + col) = v;
+                }
+                __syncwarp();
             }
             // this thread's stores before any later TMA read of them (other CTAs)
             fence_proxy_async_global();
             tc_fence_before();
             mbar_arrive(&c.tempty[b]);
+            if (tr) {
+                const unsigned long long now = clock64();
+                w_work += now - tw;
+                tw = now;
+            }
             if (publisher) {
                 // all 128 epilogue threads have stored: publish the tile
-                if (mbar_wait(&c.tempty[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
-                              0x80000000u | static_cast<unsigned>(tl))) {
+                const bool stored = mbar_wait(&c.tempty[b], aph, abort_flag, p.status,
+                                              kWhereEpiTmemFull, 0x80000000u | static_cast<unsigned>(tl));
+                if (tr) w_stores += clock64() - tw;
+                if (stored) {
                     __threadfence();
                     if (t.kind == 0)
                         red_release_add_u32(&p.l1_done[t.row], 1u);
@@ -492,6 +544,16 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 }
             }
             __syncwarp();
+        }
+        if (tr && publisher) {
+            unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
+            o[6] = w_full;
+            o[7] = w_work;
+            o[8] = w_stores;
+            o[9] = clock64() - t0;
+            o[10] = n1;
+            o[11] = n2;
+            o[13] = globaltimer_ns();
         }
     }
 
@@ -535,11 +597,11 @@ bool make_map_3d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t mid, 
 
 int ffn_l2_block_n(int d, int requested)
 {
-    if (requested >= 32 && requested <= 256 && requested % 32 == 0) return requested;
-    // widest tile (multiple of 32) that wastes the fewest padded columns
+    if (requested >= 64 && requested <= 256 && requested % 64 == 0) return requested;
+    // widest tile (multiple of 64) that wastes the fewest padded columns
     int best = 256;
     long best_pad = LONG_MAX;
-    for (int n = 256; n >= 64; n -= 32) {
+    for (int n = 256; n >= 64; n -= 64) {
         const long pad = static_cast<long>((d + n - 1) / n) * n - d;
         if (pad < best_pad) {
             best_pad = pad;
@@ -577,14 +639,19 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.kb2 = (a.F + kBlockK - 1) / kBlockK;
     p.schedule = a.schedule;
     p.epoch = a.epoch;
+    p.trace = a.trace;
+    p.group = a.group_rows > 0 ? a.group_rows : kDefaultGroupRows;
 
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     int grid = a.num_ctas > 0 ? a.num_ctas : sms;
     if (grid > sms) grid = sms;
-    // minimum lead of Linear-1 over Linear-2 (scheduler rows): the Linear-1
-    // frontier of G CTAs spans about G / P1 rows, plus one row of margin
-    p.lead = a.lead > 0 ? a.lead : (grid + p.P1 - 1) / p.P1 + 1;
+    // minimum lead of Linear-1 over Linear-2 (scheduler rows): a raster group
+    // (every tile of a row sits below position (row + group) * P1) plus the
+    // rows the G CTAs have in flight, plus one row of margin. Never below the
+    // group size: that bound is what keeps the dependency waits deadlock-free.
+    p.lead = a.lead > 0 ? a.lead : p.group + (grid + p.P1 - 1) / p.P1 + 1;
+    if (p.lead < p.group) p.lead = p.group;
 
     CUtensorMap tx, th, tw1, tw3, tw2;
     if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, kBlockM) ||

@@ -82,7 +82,7 @@ Layout make_layout(const moe_shape_t *s)
     L.chunk_tokens = moe::dispatch_chunk_tokens(s->T, s->E);
     const size_t chunks = T == 0 ? 1 : (T + L.chunk_tokens - 1) / L.chunk_tokens;
     L.max_rows = moe::ffn_max_rows(static_cast<long>(R), s->E);
-    const size_t p2max = (d + 31) / 32;  // widest flag grid: Linear-2 tiles of 32 columns
+    const size_t p2max = (d + 63) / 64;  // widest flag grid: Linear-2 tiles of 64 columns
     L.bytes[MOE_WS_STATUS] = 16;
     L.bytes[MOE_WS_TOPK_IDX] = R * 4;
     L.bytes[MOE_WS_TOPK_GATE] = R * 4;
@@ -129,8 +129,10 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->schedule != MOE_SCHEDULE_INTERLEAVED && t->schedule != MOE_SCHEDULE_EXPERT_WAVE)
         return MOE_ERR_INVALID_ARG;
     if (t->lead_rows < 0 || t->num_ctas < 0) return MOE_ERR_INVALID_ARG;
-    if (t->l2_block_n != 0 && (t->l2_block_n < 32 || t->l2_block_n > 256 || t->l2_block_n % 32))
+    if (t->l2_block_n != 0 && (t->l2_block_n < 64 || t->l2_block_n > 256 || t->l2_block_n % 64))
         return MOE_ERR_INVALID_ARG;
+    if (t->group_rows < 0 || t->reserved != 0) return MOE_ERR_INVALID_ARG;
+    if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -159,6 +161,8 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.lead = tune ? tune->lead_rows : 0;
     a.num_ctas = tune ? tune->num_ctas : 0;
     a.l2_block_n = tune ? tune->l2_block_n : 0;
+    a.group_rows = tune ? tune->group_rows : 0;
+    a.trace = tune ? static_cast<unsigned long long *>(tune->trace) : nullptr;
     a.counters_zeroed = counters_zeroed;
     a.epoch = next_epoch();
     if (moe::encode_tiled_fn() == nullptr) return MOE_ERR_CUDA;

@@ -15,10 +15,10 @@
 // that sum.
 //
 // Block tile: BT tokens x BE >= E experts, staged through shared memory 32
-// features at a time (fp32, transposed; the next chunk is prefetched into
-// registers while the current one is used), each thread owning TM tokens x TN
-// experts. Then one warp per token runs k rounds of a shuffle arg-max over the
-// block's logits and writes idx and gates.
+// features at a time as fp32 rows (the next chunk is prefetched into registers
+// while the current one is used), each thread owning TM tokens x TN experts.
+// Then one warp per token runs k rounds of a shuffle arg-max over the block's
+// logits and writes idx and gates.
 #include <cuda_bf16.h>
 #include <float.h>
 
@@ -43,25 +43,32 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
     return __uint_as_float(bits16 << 16);
 }
 
-template <int TX, int TM, int TN, int NT>
-__global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
+// Thread layout: lane = 8 token lanes x 4 expert lanes; warps = WE along
+// experts x WT along tokens. Thread (a, b) of warp (we, wt) owns tokens
+// tb + a + 8i (i < TM) and experts eb + b + 4j (j < TN), so for any fixed i
+// (or j) the warp touches consecutive rows of the shared tiles, which are
+// padded to 36 floats a row: every 16-byte access is bank-conflict free.
+template <int TM, int TN, int WE, int WT>
+__global__ void __launch_bounds__(32 * WE * WT) route_kernel(const RouteParams p)
 {
-    constexpr int TY = NT / TX;
-    constexpr int BT = TY * TM;   // tokens per block
-    constexpr int BE = TX * TN;   // experts per block (>= E)
+    constexpr int NT = 32 * WE * WT;
+    constexpr int BT = WT * 8 * TM;  // tokens per block
+    constexpr int BE = WE * 4 * TN;  // experts per block (>= E)
     constexpr int NW = NT / 32;
-    constexpr int XV = BT * (kBK / 8);  // 16-byte vectors of x per chunk
-    constexpr int WV = BE * (kBK / 8);  // 16-byte vectors of Wr per chunk
+    constexpr int LD = kBK + 4;      // padded row (floats)
+    constexpr int XV = BT * (kBK / 8);
+    constexpr int WV = BE * (kBK / 8);
     constexpr int XPT = (XV + NT - 1) / NT;
     constexpr int WPT = (WV + NT - 1) / NT;
     extern __shared__ float rsm[];
-    float *xs = rsm;             // [kBK][BT]
-    float *ws = rsm + kBK * BT;  // [kBK][BE]
-    float *lg = rsm;             // [BT][BE + 1] (reused after the K loop)
+    float *xs = rsm;            // [BT][LD]
+    float *ws = rsm + BT * LD;  // [BE][LD]
+    float *lg = rsm;            // [BT][BE + 1] (reused after the K loop)
 
     const int tid = threadIdx.x;
-    const int tx = tid % TX;
-    const int ty = tid / TX;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int a = lane & 7, b = lane >> 3;
+    const int eb = (warp % WE) * 4 * TN, tb = (warp / WE) * 8 * TM;
     const long t0 = static_cast<long>(blockIdx.x) * BT;
 
     float acc[TM][TN];
@@ -96,18 +103,22 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
             }
         }
     };
+    auto widen = [](const uint4 &q, float4 &lo, float4 &hi) {
+        lo = make_float4(bf16_bits_to_f32(q.x & 0xFFFFu), bf16_bits_to_f32(q.x >> 16),
+                         bf16_bits_to_f32(q.y & 0xFFFFu), bf16_bits_to_f32(q.y >> 16));
+        hi = make_float4(bf16_bits_to_f32(q.z & 0xFFFFu), bf16_bits_to_f32(q.z >> 16),
+                         bf16_bits_to_f32(q.w & 0xFFFFu), bf16_bits_to_f32(q.w >> 16));
+    };
     auto stage = [&]() {
 #pragma unroll
         for (int u = 0; u < XPT; ++u) {
             const int v = tid + u * NT;
             if (v < XV) {
                 const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
-                const uint32_t w[4] = {px[u].x, px[u].y, px[u].z, px[u].w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    xs[(c8 + 2 * h) * BT + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
-                    xs[(c8 + 2 * h + 1) * BT + r] = bf16_bits_to_f32(w[h] >> 16);
-                }
+                float4 lo, hi;
+                widen(px[u], lo, hi);
+                *reinterpret_cast<float4 *>(xs + r * LD + c8) = lo;
+                *reinterpret_cast<float4 *>(xs + r * LD + c8 + 4) = hi;
             }
         }
 #pragma unroll
@@ -115,12 +126,10 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
             const int v = tid + u * NT;
             if (v < WV) {
                 const int r = v / (kBK / 8), c8 = (v % (kBK / 8)) * 8;
-                const uint32_t w[4] = {pw[u].x, pw[u].y, pw[u].z, pw[u].w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    ws[(c8 + 2 * h) * BE + r] = bf16_bits_to_f32(w[h] & 0xFFFFu);
-                    ws[(c8 + 2 * h + 1) * BE + r] = bf16_bits_to_f32(w[h] >> 16);
-                }
+                float4 lo, hi;
+                widen(pw[u], lo, hi);
+                *reinterpret_cast<float4 *>(ws + r * LD + c8) = lo;
+                *reinterpret_cast<float4 *>(ws + r * LD + c8 + 4) = hi;
             }
         }
     };
@@ -130,17 +139,25 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
         stage();
         __syncthreads();
         if (k0 + kBK < p.d) fetch(k0 + kBK);
-#pragma unroll 8
-        for (int kk = 0; kk < kBK; ++kk) {
-            float xv[TM], wv[TN];
+#pragma unroll 2
+        for (int kk = 0; kk < kBK; kk += 4) {
+            float4 xv[TM], wv[TN];
 #pragma unroll
-            for (int i = 0; i < TM; ++i) xv[i] = xs[kk * BT + ty * TM + i];
+            for (int i = 0; i < TM; ++i)
+                xv[i] = *reinterpret_cast<const float4 *>(xs + (tb + a + 8 * i) * LD + kk);
 #pragma unroll
-            for (int j = 0; j < TN; ++j) wv[j] = ws[kk * BE + tx * TN + j];
+            for (int j = 0; j < TN; ++j)
+                wv[j] = *reinterpret_cast<const float4 *>(ws + (eb + b + 4 * j) * LD + kk);
+            // ascending feature order for every (token, expert) accumulator
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+                for (int j = 0; j < TN; ++j) {
+                    acc[i][j] = fmaf(xv[i].x, wv[j].x, acc[i][j]);
+                    acc[i][j] = fmaf(xv[i].y, wv[j].y, acc[i][j]);
+                    acc[i][j] = fmaf(xv[i].z, wv[j].z, acc[i][j]);
+                    acc[i][j] = fmaf(xv[i].w, wv[j].w, acc[i][j]);
+                }
         }
         __syncthreads();
     }
@@ -150,15 +167,14 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
     for (int i = 0; i < TM; ++i) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
-            const int e = tx * TN + j;
+            const int e = eb + b + 4 * j;
             float z = acc[i][j];
             if (p.bias != nullptr && e < p.E) z = z + p.bias[e];
-            lg[(ty * TM + i) * (BE + 1) + e] = z;
+            lg[(tb + a + 8 * i) * (BE + 1) + e] = z;
         }
     }
     __syncthreads();
 
-    const int warp = tid / 32, lane = tid % 32;
     for (int r = warp; r < BT; r += NW) {
         const long t = t0 + r;
         if (t >= p.T) break;
@@ -213,24 +229,25 @@ __global__ void __launch_bounds__(NT) route_kernel(const RouteParams p)
     }
 }
 
-template <int TX, int TM, int TN, int NT>
+template <int TM, int TN, int WE, int WT>
 cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
 {
-    constexpr int BT = (NT / TX) * TM;
-    constexpr int BE = TX * TN;
-    constexpr size_t stage = sizeof(float) * kBK * (BT + BE);
+    constexpr int NT = 32 * WE * WT;
+    constexpr int BT = WT * 8 * TM;
+    constexpr int BE = WE * 4 * TN;
+    constexpr size_t stage = sizeof(float) * (kBK + 4) * (BT + BE);
     constexpr size_t logits = sizeof(float) * BT * (BE + 1);
     constexpr size_t smem = stage > logits ? stage : logits;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel<TX, TM, TN, NT>,
+        cudaError_t e = cudaFuncSetAttribute(route_kernel<TM, TN, WE, WT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
-    route_kernel<TX, TM, TN, NT><<<grid, NT, smem, s>>>(p);
+    route_kernel<TM, TN, WE, WT><<<grid, NT, smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -240,14 +257,14 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
 {
     if (a.T == 0) return cudaSuccess;
     RouteParams p{a.x, a.wr, a.bias, a.topk_idx, a.topk_gate, a.T, a.d, a.E, a.k};
-    // thread tile TM tokens x TN experts; a block covers every expert and
-    // 32 tokens (64 when E > 128), so even small T gives a few blocks per SM
-    if (a.E > 128) return launch_variant<32, 8, 8, 256>(p, s);
-    if (a.E > 64) return launch_variant<32, 4, 4, 256>(p, s);
-    if (a.E > 32) return launch_variant<16, 2, 4, 256>(p, s);
-    if (a.E > 16) return launch_variant<16, 2, 2, 256>(p, s);
-    if (a.E > 8) return launch_variant<16, 2, 1, 256>(p, s);
-    return launch_variant<8, 1, 1, 256>(p, s);
+    // <TM, TN, WE, WT>: a block covers every expert (BE = 4*WE*TN >= E) and
+    // BT = 8*WT*TM tokens; small token tiles keep the 152 SMs evenly loaded
+    if (a.E > 128) return launch_variant<8, 8, 8, 1>(p, s);  // BT 64, BE 256
+    if (a.E > 64) return launch_variant<2, 8, 4, 2>(p, s);   // BT 32, BE 128
+    if (a.E > 32) return launch_variant<2, 4, 4, 1>(p, s);   // BT 16, BE 64
+    if (a.E > 16) return launch_variant<2, 2, 4, 2>(p, s);   // BT 32, BE 32
+    if (a.E > 8) return launch_variant<2, 1, 4, 2>(p, s);    // BT 32, BE 16
+    return launch_variant<1, 1, 2, 4>(p, s);                 // BT 32, BE 8
 }
 
 }  // namespace moe

@@ -72,9 +72,15 @@ typedef enum {
 
 typedef struct {
     int schedule;   /* moe_schedule_t */
-    int lead_rows;  /* D: minimum lead of Linear-1 over Linear-2 in scheduler rows; 0 = default */
+    int lead_rows;  /* D: minimum lead of Linear-1 over Linear-2 in scheduler rows; 0 = default;
+                       raised to group_rows if smaller (needed for deadlock freedom) */
     int num_ctas;   /* persistent grid size; 0 = number of SMs */
-    int l2_block_n; /* Linear-2 tile width (32..256, multiple of 32); 0 = default */
+    int l2_block_n; /* Linear-2 tile width (64, 128, 192 or 256); 0 = default */
+    int group_rows; /* raster group: an expert's tiles run N-tile-major over groups of this many
+                       128-row M-tiles, so each weight tile is reused while hot in L2; 0 = default */
+    int reserved;   /* must be 0 */
+    void *trace;    /* optional device buffer of num_ctas x 16 uint64 per-CTA counters (wait
+                       cycles per role, tile counts, start/end times); NULL = off */
 } moe_tuning_t;
 
 /* Human-readable name of a status code. Never NULL. */
