@@ -326,15 +326,24 @@ def run_ours(args, cfg):
     gemm_ms = float(stage_ms[:, 2].mean())
     gemm_flops = cfg.gemm_flops()
     achieved = gemm_flops / (gemm_ms / 1000.0) / 1e12
-    peak = float(peaks["bf16_tflops"])
+    burst = float(peaks["bf16_tflops"])
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    # the GEMM runs inside a timed loop of back-to-back layers: when that loop
+    # lasts a second or more the power-capped sustained rate is the ceiling
+    long_run = (total_ms / 1000.0) >= 1.0
+    peak = sustained if long_run else burst
     traffic = traffic_record(cfg.name)
+    kind = "sustained" if long_run else "burst"
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic, "kernel": "grouped_swiglu_gemm",
-                "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"
-                if peak_src == "measured" else "fallback 1.9 PFLOP/s"}
+                "frac": achieved / peak, "frac_of_burst": achieved / burst, "traffic": traffic,
+                "kernel": "grouped_swiglu_gemm",
+                "peak_source": (f"{peak_src} bf16 dense {kind} (MEASURED_PEAKS.json)"
+                                if peak_src == "measured" else f"fallback bf16 {kind}")}
     hbm = float(peaks["hbm_gbs"])
     t_roof = max(cfg.flops() / (peak * 1e12), cfg.minimal_bytes() / (hbm * 1e9))
+    t_roof_burst = max(cfg.flops() / (burst * 1e12), cfg.minimal_bytes() / (hbm * 1e9))
     layer_frac = t_roof / (ms_per_step / 1000.0)
+    layer_frac_burst = t_roof_burst / (ms_per_step / 1000.0)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -352,7 +361,7 @@ def run_ours(args, cfg):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(cfg, args.schedule),
         "tflops": cfg.flops() / (ms_per_step / 1000.0) / 1e12 * world,
-        "layer_roofline_frac": layer_frac,
+        "layer_roofline_frac": layer_frac, "layer_roofline_frac_of_burst": layer_frac_burst,
         "stage_ms": {"route": float(stage_ms[:, 0].mean()), "dispatch": float(stage_ms[:, 1].mean()),
                      "grouped_gemm": gemm_ms, "combine": float(stage_ms[:, 3].mean())},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

@@ -52,7 +52,7 @@ class _CShape(ctypes.Structure):
 
 class _CTuning(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int), ("lead_rows", ctypes.c_int), ("num_ctas", ctypes.c_int),
-                ("l2_block_n", ctypes.c_int), ("group_rows", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("l2_block_n", ctypes.c_int), ("group_rows", ctypes.c_int), ("cta_group", ctypes.c_int),
                 ("trace", ctypes.c_void_p)]
 
 
@@ -86,12 +86,13 @@ class Tuning:
     num_ctas: int = 0
     l2_block_n: int = 0
     group_rows: int = 0
+    cta_group: int = 0
     trace: object = None  # optional torch int64 CUDA tensor of >= num_ctas * TRACE_WORDS entries
 
     def c(self) -> _CTuning:
         tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
         return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
-                        0, tr)
+                        self.cta_group, tr)
 
 
 _lib = None

@@ -28,9 +28,17 @@
 //
 // CTA roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
 // allocator + single-thread MMA issuer, warps 2..5 = epilogue (warp w reads
-// tensor-memory lanes 32*(w%4)...+31). Shared memory holds a 4-stage ring of
-// (A 128x64, B 256x64) bf16 tiles in the 128-byte-swizzled K-major layout;
-// tensor memory holds two 128x256 fp32 accumulators (512 columns).
+// tensor-memory lanes 32*(w%4)...+31). Tensor memory holds two 128 x 256 fp32
+// accumulators (512 columns).
+//
+// CTA pairs (CG = 2, the default): the two CTAs of a cluster compute 256-row
+// tiles with tcgen05.mma.cta_group::2. Each CTA loads its own 128 rows of A and
+// half of B (Linear-1: W1 in the first CTA, W3 in the second; Linear-2: half of
+// the W2 rows), so a pipeline stage is 32 KiB and six stages fit. The first CTA
+// issues every MMA and multicasts each completion to both CTAs; both CTAs'
+// TMA loads complete on the first CTA's stage barrier; both CTAs' epilogues
+// release an accumulator by arriving on the first CTA's barrier. CG = 1 keeps
+// one CTA per tile (4 stages of 48 KiB) for comparison.
 #include <climits>
 
 #include "kernels.cuh"
@@ -39,19 +47,24 @@
 namespace moe {
 namespace {
 
-constexpr int kBlockM = 128;
-constexpr int kBlockK = 64;  // 64 bf16 = 128 B = one swizzle atom row
-constexpr int kL1N = 128;    // h columns per Linear-1 tile (MMA N = 2 * 128)
-constexpr int kStages = 4;
+constexpr int kBlockM = 128;  // rows per CTA
+constexpr int kBlockK = 64;   // 64 bf16 = 128 B = one swizzle atom row
+constexpr int kL1N = 128;     // h columns per Linear-1 tile (MMA N = 2 * 128)
 constexpr int kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
-constexpr int kBTileBytes = 256 * kBlockK * 2;      // 32 KiB
-constexpr int kL1StageBytes = kATileBytes + kBTileBytes;
-constexpr int kDefaultGroupRows = 32;
+constexpr int kMaxStages = 6;
+constexpr int kDefaultGroupRows = 32;  // raster group, in 128-row M-tiles
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kTraceWords = 16;  // per-CTA counters when tracing is on
+
+template <int CG>
+struct Cfg {
+    static constexpr int kStages = CG == 2 ? 6 : 4;
+    static constexpr int kBTileBytes = (256 / CG) * kBlockK * 2;  // this CTA's share of B
+    static constexpr int kTileRows = kBlockM * CG;                // rows of one scheduler row
+};
 
 struct GemmParams {
     const int32_t *offsets;
@@ -63,16 +76,17 @@ struct GemmParams {
     int E, d, F, R;
     int P1, P2, N2;
     int kb1, kb2;
-    int schedule, lead, group;
+    int schedule, lead, group, cg;
     unsigned epoch;
     unsigned long long *trace;
 };
 
 struct SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t full[kMaxStages];   // stage loaded (used in the pair's first CTA)
+    uint64_t empty[kMaxStages];  // stage consumed by the MMAs
+    uint64_t tfull[2];           // accumulator ready for the epilogue
+    uint64_t tempty[2];          // accumulator drained (every epilogue thread of the pair)
+    uint64_t estore[2];          // this CTA's epilogue stores issued (publisher)
     uint32_t tmem_base;
     int abort;
     int nwaves;
@@ -85,8 +99,12 @@ struct SmemCtl {
 // epilogue transpose buffer: per epilogue warp, 32 rows x 64 bf16 (128 B a row)
 constexpr int kEpiStageBytes = 32 * 128;
 constexpr size_t kCtlBytes = (sizeof(SmemCtl) + 127) / 128 * 128;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * (kATileBytes + kBTileBytes) +
-                              kCtlBytes + 4 * kEpiStageBytes;
+template <int CG>
+constexpr size_t smem_bytes()
+{
+    return 1024 /*alignment slack*/ + size_t(Cfg<CG>::kStages) * (kATileBytes + Cfg<CG>::kBTileBytes) +
+           kCtlBytes + 4 * kEpiStageBytes;
+}
 
 struct Tile {
     int kind;  // 0 = Linear-1, 1 = Linear-2, -1 = no more tiles
@@ -140,14 +158,14 @@ struct Scheduler {
         const long P = c.row_start[p.E];
         P1 = p.P1;
         P2 = p.P2;
-        G = gridDim.x;
+        G = gridDim.x / p.cg;
         D = p.lead;
         GM = p.group;
         mode = p.schedule;
-        k1 = k2 = blockIdx.x;
+        k1 = k2 = blockIdx.x / p.cg;
         tot1 = P * P1;
         tot2 = P * P2;
-        gi = blockIdx.x;
+        gi = blockIdx.x / p.cg;
         w = 0;
     }
 
@@ -225,6 +243,7 @@ __device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits)
     return g * __fdividef(1.0f, 1.0f + __expf(-g)) * u;
 }
 
+template <int CG>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_h,
@@ -235,6 +254,9 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     extern __shared__ uint8_t smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
     uint8_t *sA = reinterpret_cast<uint8_t *>(base);
+    constexpr int kStages = Cfg<CG>::kStages;
+    constexpr int kBTileBytes = Cfg<CG>::kBTileBytes;
+    constexpr int kTileRows = Cfg<CG>::kTileRows;
     uint8_t *sB = sA + kStages * kATileBytes;
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(sB + kStages * kBTileBytes);
     uint8_t *s_epi = sB + kStages * kBTileBytes + kCtlBytes;
@@ -242,6 +264,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int E = p.E;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // CTA within the pair
+    const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -250,7 +274,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&c.tfull[b], 1);
-            mbar_init(&c.tempty[b], kEpiThreads);
+            mbar_init(&c.tempty[b], kEpiThreads * CG);
+            mbar_init(&c.estore[b], kEpiThreads);
         }
         c.abort = 0;
         fence_barrier_init();
@@ -263,8 +288,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         tma_prefetch_desc(&tm_w2);
     }
     if (warp == 1) {
-        tmem_alloc(&c.tmem_base, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<CG>(&c.tmem_base, kTmemCols);
+        tmem_relinquish<CG>();
         tc_fence_before();
     }
     if (warp == 2) {
@@ -281,7 +306,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 c.offs[e] = o0;
                 if (e == E - 1) c.offs[E] = o1;
                 bad |= o1 < o0 || (e == 0 && o0 != 0) || (e == E - 1 && o1 != p.R);
-                local += (o1 - o0 + kBlockM - 1) / kBlockM;
+                local += (o1 - o0 + kTileRows - 1) / kTileRows;
             }
         }
         const bool any_bad = __any_sync(0xffffffffu, bad);
@@ -301,7 +326,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int e = lane * per + i;
             if (e < E) {
                 c.row_start[e] = run;
-                if (!any_bad) run += (c.offs[e + 1] - c.offs[e] + kBlockM - 1) / kBlockM;
+                if (!any_bad) run += (c.offs[e + 1] - c.offs[e] + kTileRows - 1) / kTileRows;
             }
         }
         if (lane == 31) c.row_start[E] = incl;
@@ -316,7 +341,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             int wr = 0;
             for (int e = 0; e < E; ++e) {
                 const int r1 = c.row_start[e + 1];
-                if (static_cast<long>(r1 - wr) * p.P1 >= gridDim.x || e == E - 1) {
+                if (static_cast<long>(r1 - wr) * p.P1 >= gridDim.x / CG || e == E - 1) {
                     tiles += static_cast<long>(r1 - wr) * (p.P1 + p.P2);
                     ++nw;
                     c.wave_row[nw] = r1;
@@ -328,6 +353,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
     }
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync_all();  // the peer's barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = c.tmem_base;
     volatile int *abort_flag = &c.abort;
@@ -345,18 +371,22 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 const Tile t = sch.next(c, E);
                 if (t.kind < 0) break;
                 const int e = row_expert(c, E, t.row);
-                const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kBlockM;
+                // this CTA's 128 rows of the scheduler row
+                const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows +
+                                 static_cast<int>(rank) * kBlockM;
                 if (t.kind == 1) {
                     const unsigned long long tw = tr ? clock64() : 0;
-                    if (!wait_rows_ready(&p.l1_done[t.row], static_cast<unsigned>(p.P1), abort_flag,
-                                         p.status, static_cast<unsigned>(t.row)))
+                    if (!wait_rows_ready(&p.l1_done[t.row], static_cast<unsigned>(CG * p.P1),
+                                         abort_flag, p.status, static_cast<unsigned>(t.row)))
                         break;
                     if (tr) w_rows += clock64() - tw;
                     fence_proxy_async_global();
                 }
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
+                // bytes of one stage summed over the CTAs of the pair
                 const uint32_t bytes =
-                    t.kind == 0 ? kL1StageBytes : kATileBytes + p.N2 * kBlockK * 2;
+                    CG * (t.kind == 0 ? kATileBytes + kBTileBytes
+                                      : kATileBytes + (p.N2 / CG) * kBlockK * 2);
                 for (int kb = 0; kb < nkb; ++kb) {
                     const unsigned long long tw = tr ? clock64() : 0;
                     if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag, p.status, kWhereProducerEmpty,
@@ -365,17 +395,23 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         break;
                     }
                     if (tr) w_empty += clock64() - tw;
-                    mbar_arrive_expect_tx(&c.full[s], bytes);
+                    // the pair's loads all complete on the first CTA's barrier
+                    if (leader) mbar_arrive_expect_tx(&c.full[s], bytes);
+                    const uint32_t bar = CG == 2 ? map_to_cta(smem_u32(&c.full[s]), 0)
+                                                 : smem_u32(&c.full[s]);
                     uint8_t *a = sA + s * kATileBytes;
                     uint8_t *b = sB + s * kBTileBytes;
                     if (t.kind == 0) {
-                        tma_load_2d(&tm_x, &c.full[s], a, kb * kBlockK, row0);
-                        tma_load_3d(&tm_w1, &c.full[s], b, kb * kBlockK, t.n * kL1N, e);
-                        tma_load_3d(&tm_w3, &c.full[s], b + kBTileBytes / 2, kb * kBlockK,
-                                    t.n * kL1N, e);
+                        tma_load_2d<CG>(&tm_x, bar, a, kb * kBlockK, row0);
+                        if (CG == 1 || rank == 0)
+                            tma_load_3d<CG>(&tm_w1, bar, b, kb * kBlockK, t.n * kL1N, e);
+                        if (CG == 1 || rank == 1)
+                            tma_load_3d<CG>(&tm_w3, bar, CG == 1 ? b + kBTileBytes / 2 : b,
+                                            kb * kBlockK, t.n * kL1N, e);
                     } else {
-                        tma_load_2d(&tm_h, &c.full[s], a, kb * kBlockK, row0);
-                        tma_load_3d(&tm_w2, &c.full[s], b, kb * kBlockK, t.n * p.N2, e);
+                        tma_load_2d<CG>(&tm_h, bar, a, kb * kBlockK, row0);
+                        tma_load_3d<CG>(&tm_w2, bar, b, kb * kBlockK,
+                                        t.n * p.N2 + static_cast<int>(rank) * (p.N2 / CG), e);
                     }
                     if (++s == kStages) {
                         s = 0;
@@ -392,12 +428,12 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             Scheduler sch(c, p);
             int s = 0;
             uint32_t ph = 0;
-            const uint32_t idesc1 = idesc_bf16_f32(kBlockM, 2 * kL1N);
-            const uint32_t idesc2 = idesc_bf16_f32(kBlockM, p.N2);
+            const uint32_t idesc1 = idesc_bf16_f32(kTileRows, 2 * kL1N);
+            const uint32_t idesc2 = idesc_bf16_f32(kTileRows, p.N2);
             bool ok = true;
             unsigned long long w_full = 0, w_tmem = 0, t0 = tr ? clock64() : 0;
             for (int tl = 0; ok; ++tl) {
@@ -428,16 +464,16 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         // advance 16 bf16 (32 B) along K inside the swizzle atom
-                        mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
+                        mma_bf16_ss<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
+                                        (kb | kk) != 0 ? 1u : 0u);
                     }
-                    mma_commit(&c.empty[s]);
+                    mma_commit<CG>(&c.empty[s]);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
-                if (ok) mma_commit(&c.tfull[b]);
+                if (ok) mma_commit<CG>(&c.tfull[b]);
             }
             if (tr) {
                 unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
@@ -472,8 +508,9 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             }
             tc_fence_after();
             const int e = row_expert(c, E, t.row);
-            const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kBlockM;
-            const int valid_rows = min(kBlockM, c.offs[e + 1] - row0);
+            const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows +
+                             static_cast<int>(rank) * kBlockM;
+            const int valid_rows = min(kBlockM, c.offs[e + 1] - row0);  // may be <= 0
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(b) * kAccCols;
             // 64 columns at a time: tensor memory -> registers (thread = row) ->
@@ -523,7 +560,11 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             // this thread's stores before any later TMA read of them (other CTAs)
             fence_proxy_async_global();
             tc_fence_before();
-            mbar_arrive(&c.tempty[b]);
+            mbar_arrive(&c.estore[b]);
+            if constexpr (CG == 2)
+                mbar_arrive_cluster(map_to_cta(smem_u32(&c.tempty[b]), 0));
+            else
+                mbar_arrive(&c.tempty[b]);
             if (tr) {
                 const unsigned long long now = clock64();
                 w_work += now - tw;
@@ -531,7 +572,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             }
             if (publisher) {
                 // all 128 epilogue threads have stored: publish the tile
-                const bool stored = mbar_wait(&c.tempty[b], aph, abort_flag, p.status,
+                const bool stored = mbar_wait(&c.estore[b], aph, abort_flag, p.status,
                                               kWhereEpiTmemFull, 0x80000000u | static_cast<unsigned>(tl));
                 if (tr) w_stores += clock64() - tw;
                 if (stored) {
@@ -539,8 +580,9 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                     if (t.kind == 0)
                         red_release_add_u32(&p.l1_done[t.row], 1u);
                     else
-                        st_release_u32(&p.l2_flags[static_cast<long>(t.row) * p.P2 + t.n],
-                                       p.epoch);
+                        st_release_u32(
+                            &p.l2_flags[(static_cast<long>(t.row) * p.P2 + t.n) * CG + rank],
+                            p.epoch);
                 }
             }
             __syncwarp();
@@ -559,9 +601,10 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync_all();  // the pair is done with both CTAs' tensor memory
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc<CG>(tmem_base, kTmemCols);
     }
 }
 
@@ -613,14 +656,81 @@ int ffn_l2_block_n(int d, int requested)
 
 long ffn_max_rows(long R, int E)
 {
-    // sum_e ceil(c_e / 128) <= R / 128 + E
-    return R / kBlockM + E + 1;
+    // 128-row M-tiles: sum_e ceil(c_e / 128) <= R / 128 + E; CTA pairs use
+    // (R / 256 + E) scheduler rows with two flags per Linear-2 tile
+    return R / kBlockM + 2L * E + 2;
 }
+
+namespace {
+
+template <int CG>
+cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
+{
+    constexpr size_t smem = smem_bytes<CG>();
+    static bool attr_set = false;
+    static int max_instances = 0;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!attr_set) {
+        cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel<CG>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        // every CTA of the persistent grid must be resident at once (the
+        // Linear-2 tiles wait on Linear-1 tiles of other CTAs)
+        int clusters = 0;
+        cfg.gridDim = dim3(static_cast<unsigned>(sms / CG * CG), 1, 1);
+        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG>, &cfg);
+        if (err != cudaSuccess) return err;
+        max_instances = clusters < sms / CG ? clusters : sms / CG;
+        if (max_instances <= 0) return cudaErrorInvalidConfiguration;
+        attr_set = true;
+    }
+    int instances = max_instances;
+    if (a.num_ctas > 0) {
+        const int want = a.num_ctas / CG > 0 ? a.num_ctas / CG : 1;
+        if (want < instances) instances = want;
+    }
+    // minimum lead of Linear-1 over Linear-2 (scheduler rows): a raster group
+    // (every tile of a row sits below position (row + group) * P1) plus the
+    // rows the instances have in flight, plus one row of margin. Never below
+    // the group size: that bound keeps the dependency waits deadlock-free.
+    p.lead = a.lead > 0 ? a.lead : p.group + (instances + p.P1 - 1) / p.P1 + 1;
+    if (p.lead < p.group) p.lead = p.group;
+
+    const long R = a.R;
+    CUtensorMap tx, th, tw1, tw3, tw2;
+    if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, kBlockM) ||
+        !make_map_2d(&th, a.h, a.F, R, kBlockK, kBlockM) ||
+        !make_map_3d(&tw1, a.w1, a.d, a.F, a.E, kBlockK, kL1N) ||
+        !make_map_3d(&tw3, a.w3, a.d, a.F, a.E, kBlockK, kL1N) ||
+        !make_map_3d(&tw2, a.w2, a.F, a.d, a.E, kBlockK, p.N2 / CG))
+        return cudaErrorInvalidValue;
+
+    if (!a.counters_zeroed) {
+        cudaError_t err = cudaMemsetAsync(a.l1_done, 0, sizeof(unsigned) * a.max_rows, stream);
+        if (err != cudaSuccess) return err;
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(instances * CG), 1, 1);
+    return cudaLaunchKernelEx(&cfg, grouped_swiglu_gemm_kernel<CG>, tx, th, tw1, tw3, tw2, p);
+}
+
+}  // namespace
 
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
 {
-    const long R = a.R;
-    if (R == 0) return cudaSuccess;
+    if (a.R == 0) return cudaSuccess;
     GemmParams p;
     p.offsets = a.offsets;
     p.h = a.h;
@@ -640,41 +750,16 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.schedule = a.schedule;
     p.epoch = a.epoch;
     p.trace = a.trace;
-    p.group = a.group_rows > 0 ? a.group_rows : kDefaultGroupRows;
-
-    const int sms = device_sm_count();
-    if (sms <= 0) return cudaErrorInvalidDevice;
-    int grid = a.num_ctas > 0 ? a.num_ctas : sms;
-    if (grid > sms) grid = sms;
-    // minimum lead of Linear-1 over Linear-2 (scheduler rows): a raster group
-    // (every tile of a row sits below position (row + group) * P1) plus the
-    // rows the G CTAs have in flight, plus one row of margin. Never below the
-    // group size: that bound is what keeps the dependency waits deadlock-free.
-    p.lead = a.lead > 0 ? a.lead : p.group + (grid + p.P1 - 1) / p.P1 + 1;
-    if (p.lead < p.group) p.lead = p.group;
-
-    CUtensorMap tx, th, tw1, tw3, tw2;
-    if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, kBlockM) ||
-        !make_map_2d(&th, a.h, a.F, R, kBlockK, kBlockM) ||
-        !make_map_3d(&tw1, a.w1, a.d, a.F, a.E, kBlockK, kL1N) ||
-        !make_map_3d(&tw3, a.w3, a.d, a.F, a.E, kBlockK, kL1N) ||
-        !make_map_3d(&tw2, a.w2, a.F, a.d, a.E, kBlockK, p.N2))
-        return cudaErrorInvalidValue;
-
-    if (!a.counters_zeroed) {
-        cudaError_t err = cudaMemsetAsync(a.l1_done, 0, sizeof(unsigned) * a.max_rows, stream);
-        if (err != cudaSuccess) return err;
-    }
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kSmemBytes));
-        if (err != cudaSuccess) return err;
-        attr_set = true;
-    }
-    grouped_swiglu_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tx, th, tw1, tw3, tw2, p);
-    return cudaGetLastError();
+    // CTA pairs halve the operand traffic per MMA but pad every expert to
+    // 256-row tiles; below ~1024 rows per expert the padding costs more
+    if (a.cta_group == 1 || a.cta_group == 2)
+        p.cg = a.cta_group;
+    else
+        p.cg = a.R / a.E >= 1024 ? 2 : 1;
+    const int group = a.group_rows > 0 ? a.group_rows : kDefaultGroupRows;  // 128-row M-tiles
+    p.group = (group + p.cg - 1) / p.cg;                                     // scheduler rows
+    if (p.cg == 1) return launch_cg<1>(a, p, stream);
+    return launch_cg<2>(a, p, stream);
 }
 
 }  // namespace moe

@@ -53,7 +53,7 @@ struct FfnArgs {
     unsigned *status;        // 4 words
     long max_rows;
     int R, d, F, E;
-    int schedule, lead, num_ctas, l2_block_n, group_rows;
+    int schedule, lead, num_ctas, l2_block_n, group_rows, cta_group;
     unsigned long long *trace;  // optional per-CTA counters (16 per CTA)
     bool counters_zeroed;    // l1_done already cleared by an earlier kernel on the stream
     unsigned epoch;

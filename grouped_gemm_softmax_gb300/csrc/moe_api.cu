@@ -131,7 +131,7 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->lead_rows < 0 || t->num_ctas < 0) return MOE_ERR_INVALID_ARG;
     if (t->l2_block_n != 0 && (t->l2_block_n < 64 || t->l2_block_n > 256 || t->l2_block_n % 64))
         return MOE_ERR_INVALID_ARG;
-    if (t->group_rows < 0 || t->reserved != 0) return MOE_ERR_INVALID_ARG;
+    if (t->group_rows < 0 || t->cta_group < 0 || t->cta_group > 2) return MOE_ERR_INVALID_ARG;
     if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
@@ -162,6 +162,7 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.num_ctas = tune ? tune->num_ctas : 0;
     a.l2_block_n = tune ? tune->l2_block_n : 0;
     a.group_rows = tune ? tune->group_rows : 0;
+    a.cta_group = tune ? tune->cta_group : 0;
     a.trace = tune ? static_cast<unsigned long long *>(tune->trace) : nullptr;
     a.counters_zeroed = counters_zeroed;
     a.epoch = next_epoch();

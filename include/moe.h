@@ -74,11 +74,13 @@ typedef struct {
     int schedule;   /* moe_schedule_t */
     int lead_rows;  /* D: minimum lead of Linear-1 over Linear-2 in scheduler rows; 0 = default;
                        raised to group_rows if smaller (needed for deadlock freedom) */
-    int num_ctas;   /* persistent grid size; 0 = number of SMs */
+    int num_ctas;   /* persistent grid size in CTAs (rounded down to whole CTA groups); 0 = as
+                       many as are co-resident (one per SM) */
     int l2_block_n; /* Linear-2 tile width (64, 128, 192 or 256); 0 = default */
     int group_rows; /* raster group: an expert's tiles run N-tile-major over groups of this many
                        128-row M-tiles, so each weight tile is reused while hot in L2; 0 = default */
-    int reserved;   /* must be 0 */
+    int cta_group;  /* CTAs per MMA tile: 2 = CTA pairs with 256-row tiles, 1 = single CTAs
+                       with 128-row tiles; 0 = default (pairs when T*k/E >= 1024) */
     void *trace;    /* optional device buffer of num_ctas x 16 uint64 per-CTA counters (wait
                        cycles per role, tile counts, start/end times); NULL = off */
 } moe_tuning_t;

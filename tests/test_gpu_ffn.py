@@ -70,17 +70,34 @@ def test_ffn_parity(name):
     assert_close(to_f64(y), yref, f"{name} y")
 
 
-def test_ffn_schedules_and_grids_are_bit_identical():
+@pytest.mark.parametrize("cg", [1, 2])
+def test_ffn_schedules_and_grids_are_bit_identical(cg):
+    """The tile order never changes a result: every schedule, lead, raster group
+    and grid size gives the same bits (within one CTA-group size)."""
     need_gpu()
     c = make_case([70, 0, 129, 1, 255, 57, 300, 12] * 4, 256, 384, seed=9)
-    _, _, h0, y0 = run_ffn(c)
-    variants = [moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE), moe.Tuning(lead_rows=1),
-                moe.Tuning(lead_rows=50), moe.Tuning(num_ctas=1), moe.Tuning(num_ctas=7),
-                moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE, num_ctas=3)]
-    for t in variants:
+    _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(cta_group=cg))
+    variants = [dict(schedule=moe.SCHEDULE_EXPERT_WAVE), dict(lead_rows=1), dict(lead_rows=50),
+                dict(num_ctas=2), dict(num_ctas=7), dict(group_rows=1), dict(group_rows=4),
+                dict(schedule=moe.SCHEDULE_EXPERT_WAVE, num_ctas=6, group_rows=2)]
+    for v in variants:
+        t = moe.Tuning(cta_group=cg, **v)
         _, _, h, y = run_ffn(c, tuning=t)
         assert torch.equal(h.view(torch.int16), h0.view(torch.int16)), t
         assert torch.equal(y.view(torch.int16), y0.view(torch.int16)), t
+
+
+def test_cta_pairs_match_single_ctas():
+    need_gpu()
+    c = make_case([70, 0, 129, 1, 255, 57, 300, 12], 256, 384, seed=10)
+    _, _, h1, y1 = run_ffn(c, tuning=moe.Tuning(cta_group=1))
+    _, _, h2, y2 = run_ffn(c, tuning=moe.Tuning(cta_group=2))
+    href, yref = oracle_rows(c, np.arange(c["R"]))
+    assert_close(to_f64(h2), href, "pairs h")
+    assert_close(to_f64(y2), yref, "pairs y")
+    # the same MMA arithmetic per element: expected bit-identical
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
 
 
 @pytest.mark.parametrize("n2", [64, 128, 192, 256])
@@ -92,17 +109,32 @@ def test_ffn_l2_tile_widths(n2):
     assert_close(to_f64(y), yref, f"N2={n2} y")
 
 
-def test_ready_flags_carry_the_call_epoch():
+@pytest.mark.parametrize("cg", [1, 2])
+def test_ready_flags_carry_the_call_epoch(cg):
     need_gpu()
     counts = [70, 0, 129, 1, 255]
     c = make_case(counts, 256, 256, seed=4)
-    s, ws, _, _ = run_ffn(c)
-    rows = int(sum((n + 127) // 128 for n in counts))
+    t = moe.Tuning(cta_group=cg)
+    s, ws, _, _ = run_ffn(c, tuning=t)
+    rows = int(sum((n + 128 * cg - 1) // (128 * cg) for n in counts))  # scheduler rows
     p2 = 1  # d = 256 -> one 256-wide Linear-2 tile per row
-    flags = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (rows * p2,)).cpu().numpy()
+    nflags = rows * p2 * cg  # one flag per CTA of each Linear-2 tile
+    flags = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (nflags,)).cpu().numpy()
     assert flags[0] != 0 and np.all(flags == flags[0])
     done = moe.ws_view(ws, s, moe.WS.L1_DONE, torch.int32, (rows,)).cpu().numpy()
-    assert np.all(done == 2)  # F = 256 -> two Linear-1 tiles per row
-    run_ffn(c, ws=ws)
-    flags2 = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (rows * p2,)).cpu().numpy()
+    assert np.all(done == 2 * cg)  # F = 256 -> two Linear-1 tiles per row, one count per CTA
+    run_ffn(c, tuning=t, ws=ws)
+    flags2 = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (nflags,)).cpu().numpy()
     assert np.all(flags2 == flags2[0]) and flags2[0] != flags[0]
+
+
+def test_bad_expert_offsets_are_reported_not_computed():
+    need_gpu()
+    c = make_case([100, 50], 64, 64, seed=5)
+    c["offsets"] = np.array([0, 120, 100], np.int32)  # decreasing: invalid
+    s = moe.Shape(T=c["R"], d=c["d"], E=c["E"], top_k=1, ffn=c["F"])
+    ws = moe.alloc_workspace(s)
+    y = torch.full((c["R"], c["d"]), 7.0, dtype=torch.bfloat16, device="cuda")
+    moe.expert_ffn(s, c["x"], torch.from_numpy(c["offsets"]).cuda(), c["w1"], c["w3"], c["w2"], y, ws)
+    assert moe.last_device_status(ws) == moe.MOE_ERR_INVALID_ARG
+    assert torch.all(y == 7.0)  # nothing was written
