@@ -138,6 +138,30 @@ moe_status_t moe_dispatch(const moe_shape_t *shape, const moe_bf16_t *x, const i
                           int32_t *slot_of_row, moe_bf16_t *x_perm, void *ws, size_t ws_bytes,
                           moe_stream_t stream);
 
+/* moe_dispatch without a workspace. The pages have no counterpart to this
+ * call; it exists for callers that cannot allocate device memory for the
+ * library: a host application that owns every device buffer and passes only
+ * the tensors it already holds, or a latency-critical loop that must not call
+ * cudaMalloc (which can synchronise the device) and has no spare memory budget.
+ * Same arguments, results and rules as moe_dispatch, minus ws/ws_bytes.
+ *   - Its scratch is a fixed array inside this library's device memory: 4096
+ *     (chunk, expert) cells (16 KiB) plus 256 B of status words, present on
+ *     every GPU that loads the library until the process exits. Shapes whose
+ *     dispatch needs more cells than that (roughly T*E > 2^20 token-expert
+ *     pairs) return MOE_ERR_UNSUPPORTED without enqueuing anything.
+ *   - The first call on each device looks up that array's device address
+ *     (with the device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind: calls that overlap on the GPU (other streams, other threads)
+ *     race; serialise them.
+ *   - An expert id outside [0,E) is skipped (row_of_slot = -1, not counted)
+ *     but, with no workspace, not reported through a device status word. */
+moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const moe_bf16_t *x,
+                                  const int32_t *topk_idx, int32_t *expert_counts,
+                                  int32_t *expert_offsets, int32_t *row_of_slot,
+                                  int32_t *slot_of_row, moe_bf16_t *x_perm, moe_stream_t stream);
+
 /* Step 3, expert computation (Xian et al. section 2.2) as one persistent
  * grouped GEMM over all experts (tcgen05 MMA, bf16 in, fp32 accumulation in
  * tensor memory):
