@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--lead", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stage", choices=["route"], default=None,
+                    help="time one entry point alone (for profiling) instead of the layer")
     return ap.parse_args()
 
 
@@ -373,10 +375,42 @@ def run_ours(args, cfg):
         dist.destroy_process_group()
 
 
+def run_stage(args, cfg):
+    """Time moe_route alone on the config's x and router weights (no expert
+    weights are generated): one JSON line with the stage's mean time."""
+    import grouped_gemm_softmax_gb300 as moe
+    from grouped_gemm_softmax_gb300 import build as moe_build
+
+    if not moe_build.up_to_date():
+        moe_build.build()
+    dev = torch.device("cuda", 0)
+    shape = moe.Shape(T=cfg.T, d=cfg.d, E=cfg.E, top_k=cfg.k, ffn=cfg.F, num_segments=cfg.S)
+    inp = synth.make_inputs(cfg, seed=0, device=dev, weights=False)
+    idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+    gate = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        moe.route(shape, inp.x, inp.wr, inp.bias, idx, gate)
+        b.record()
+        if i >= args.warmup:
+            ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    print(json.dumps({"stage": args.stage, "config": workload_config(cfg, "n/a"), "ms": ms,
+                      "fp32_tflops": 2.0 * cfg.T * cfg.d * cfg.E / (ms / 1000.0) / 1e12,
+                      "steps": args.steps}), flush=True)
+
+
 def main():
     args = parse_args()
     cfg = synth.CONFIGS[args.config]
-    if args.impl == "reference":
+    if args.stage:
+        run_stage(args, cfg)
+    elif args.impl == "reference":
         run_reference(args, cfg)
     else:
         run_ours(args, cfg)
