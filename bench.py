@@ -204,6 +204,21 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's value (the job's time is its slowest rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, steps: int, world: int, slowest_ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (slowest_ms / 1000.0)
+
+
 # ----------------------------------------------------------------- our leg
 def traffic_record(cfg_name):
     """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if its
@@ -284,12 +299,8 @@ def run_ours(args, cfg):
 
     stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(4)] for evs in events])
     step_ms = stage_ms.sum(1)
-    total_ms = float(step_ms.sum())
-    if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * cfg.T * args.steps / (total_ms / 1000.0)
+    total_ms = max_over_ranks(float(step_ms.sum()), dist, dev)
+    value = job_throughput(cfg.T, args.steps, world, total_ms)
     ms_per_step = total_ms / args.steps
 
     # e2e through the same C call with host buffers: pinned H2D of x, D2H of out
@@ -311,12 +322,8 @@ def run_ours(args, cfg):
             if k >= args.warmup:
                 e2e_ms.append((a, b))
         torch.cuda.synchronize(dev)
-        e2e_total = sum(a.elapsed_time(b) for a, b in e2e_ms)
-        if dist:
-            t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_total = float(t.item())
-        e2e = {"value": world * cfg.T * args.steps / (e2e_total / 1000.0), "unit": "tokens/s",
+        e2e_total = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ms), dist, dev)
+        e2e = {"value": job_throughput(cfg.T, args.steps, world, e2e_total), "unit": "tokens/s",
                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2}
 
     if rank != 0:
