@@ -53,6 +53,7 @@ class _CShape(ctypes.Structure):
 class _CTuning(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int), ("lead_rows", ctypes.c_int), ("num_ctas", ctypes.c_int),
                 ("l2_block_n", ctypes.c_int), ("group_rows", ctypes.c_int), ("cta_group", ctypes.c_int),
+                ("wait_limit_us", ctypes.c_int), ("unmet_dependency", ctypes.c_int),
                 ("trace", ctypes.c_void_p)]
 
 
@@ -87,12 +88,14 @@ class Tuning:
     l2_block_n: int = 0
     group_rows: int = 0
     cta_group: int = 0
+    wait_limit_us: int = 0
+    unmet_dependency: int = 0
     trace: object = None  # optional torch int64 CUDA tensor of >= num_ctas * TRACE_WORDS entries
 
     def c(self) -> _CTuning:
         tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
         return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
-                        self.cta_group, tr)
+                        self.cta_group, self.wait_limit_us, self.unmet_dependency, tr)
 
 
 _lib = None

@@ -77,6 +77,8 @@ struct GemmParams {
     int P1, P2, N2;
     int kb1, kb2;
     int schedule, lead, group, cg;
+    int unmet_dependency;  // > 0 only in the failure-detection test: a wait nothing satisfies
+    unsigned long long wait_ns;  // limit of every bounded wait
     unsigned epoch;
     unsigned long long *trace;
 };
@@ -87,6 +89,7 @@ struct SmemCtl {
     uint64_t tfull[2];           // accumulator ready for the epilogue
     uint64_t tempty[2];          // accumulator drained (every epilogue thread of the pair)
     uint64_t estore[2];          // this CTA's epilogue stores issued (publisher)
+    uint64_t drain;              // every MMA this CTA issued has completed (teardown)
     uint32_t tmem_base;
     int abort;
     int nwaves;
@@ -208,7 +211,7 @@ struct Scheduler {
 
 __device__ __forceinline__ bool wait_rows_ready(const unsigned *ctr, unsigned target,
                                                 volatile int *cta_abort, unsigned *status,
-                                                unsigned detail)
+                                                unsigned detail, unsigned long long limit_ns)
 {
     if (ld_acquire_u32(ctr) >= target) return true;
     const unsigned long long t0 = globaltimer_ns();
@@ -221,7 +224,7 @@ __device__ __forceinline__ bool wait_rows_ready(const unsigned *ctr, unsigned ta
                 *cta_abort = 1;
                 return false;
             }
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 report_failure(status, kStatusTimeout, kWhereProducerDep, detail);
                 *cta_abort = 1;
                 return false;
@@ -277,6 +280,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             mbar_init(&c.tempty[b], kEpiThreads * CG);
             mbar_init(&c.estore[b], kEpiThreads);
         }
+        mbar_init(&c.drain, 1);
         c.abort = 0;
         fence_barrier_init();
     }
@@ -376,8 +380,10 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                                  static_cast<int>(rank) * kBlockM;
                 if (t.kind == 1) {
                     const unsigned long long tw = tr ? clock64() : 0;
-                    if (!wait_rows_ready(&p.l1_done[t.row], static_cast<unsigned>(CG * p.P1),
-                                         abort_flag, p.status, static_cast<unsigned>(t.row)))
+                    if (!wait_rows_ready(&p.l1_done[t.row],
+                                         static_cast<unsigned>(CG * p.P1 + p.unmet_dependency),
+                                         abort_flag, p.status, static_cast<unsigned>(t.row),
+                                         p.wait_ns))
                         break;
                     if (tr) w_rows += clock64() - tw;
                     fence_proxy_async_global();
@@ -390,7 +396,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 for (int kb = 0; kb < nkb; ++kb) {
                     const unsigned long long tw = tr ? clock64() : 0;
                     if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag, p.status, kWhereProducerEmpty,
-                                   static_cast<unsigned>(s))) {
+                                   static_cast<unsigned>(s), p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -443,7 +449,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
                 unsigned long long tw = tr ? clock64() : 0;
                 if (!mbar_wait(&c.tempty[b], aph ^ 1u, abort_flag, p.status, kWhereMmaTmemEmpty,
-                               static_cast<unsigned>(tl)))
+                               static_cast<unsigned>(tl), p.wait_ns))
                     break;
                 if (tr) w_tmem += clock64() - tw;
                 tc_fence_after();
@@ -453,7 +459,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 for (int kb = 0; kb < nkb; ++kb) {
                     tw = tr ? clock64() : 0;
                     if (!mbar_wait(&c.full[s], ph, abort_flag, p.status, kWhereMmaFull,
-                                   static_cast<unsigned>(s))) {
+                                   static_cast<unsigned>(s), p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -475,6 +481,10 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 }
                 if (ok) mma_commit<CG>(&c.tfull[b]);
             }
+            // every issued MMA must finish before tensor memory is freed, also
+            // when the loop was left early
+            mma_commit<CG>(&c.drain, 1);
+            mbar_wait_drain(&c.drain, 0, p.wait_ns);
             if (tr) {
                 unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
                 o[3] = w_full;
@@ -496,9 +506,10 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int b = tl & 1;
             const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
             unsigned long long tw = tr ? clock64() : 0;
-            if (!mbar_wait(&c.tfull[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
-                           static_cast<unsigned>(tl)))
-                break;
+            // the whole warp agrees before its warp-collective tensor-memory loads
+            const bool ready = mbar_wait(&c.tfull[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
+                                         static_cast<unsigned>(tl), p.wait_ns);
+            if (!__all_sync(0xffffffffu, ready)) break;
             if (tr) {
                 const unsigned long long now = clock64();
                 w_full += now - tw;
@@ -573,7 +584,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             if (publisher) {
                 // all 128 epilogue threads have stored: publish the tile
                 const bool stored = mbar_wait(&c.estore[b], aph, abort_flag, p.status,
-                                              kWhereEpiTmemFull, 0x80000000u | static_cast<unsigned>(tl));
+                                              kWhereEpiTmemFull, 0x80000000u | static_cast<unsigned>(tl),
+                                              p.wait_ns);
                 if (tr) w_stores += clock64() - tw;
                 if (stored) {
                     __threadfence();
@@ -599,6 +611,12 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
     }
 
+    // after an early exit, let loads that were already issued land before the
+    // CTA's shared memory is released (bounded; never taken on the normal path)
+    if (warp == 0 && lane == 0 && (*abort_flag || ld_volatile_u32(p.status) != 0u)) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
+    }
     tc_fence_before();
     __syncthreads();
     if constexpr (CG == 2) cluster_sync_all();  // the pair is done with both CTAs' tensor memory
@@ -750,6 +768,9 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.schedule = a.schedule;
     p.epoch = a.epoch;
     p.trace = a.trace;
+    p.wait_ns = a.wait_limit_us > 0 ? 1000ull * static_cast<unsigned long long>(a.wait_limit_us)
+                                    : kWaitLimitNs;
+    p.unmet_dependency = a.unmet_dependency > 0 ? 1 : 0;
     // CTA pairs halve the operand traffic per MMA but pad every expert to
     // 256-row tiles; below ~1024 rows per expert the padding costs more
     if (a.cta_group == 1 || a.cta_group == 2)

@@ -54,6 +54,7 @@ struct FfnArgs {
     long max_rows;
     int R, d, F, E;
     int schedule, lead, num_ctas, l2_block_n, group_rows, cta_group;
+    int wait_limit_us, unmet_dependency;
     unsigned long long *trace;  // optional per-CTA counters (16 per CTA)
     bool counters_zeroed;    // l1_done already cleared by an earlier kernel on the stream
     unsigned epoch;

@@ -132,6 +132,8 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->l2_block_n != 0 && (t->l2_block_n < 64 || t->l2_block_n > 256 || t->l2_block_n % 64))
         return MOE_ERR_INVALID_ARG;
     if (t->group_rows < 0 || t->cta_group < 0 || t->cta_group > 2) return MOE_ERR_INVALID_ARG;
+    if (t->wait_limit_us < 0 || t->unmet_dependency < 0 || t->unmet_dependency > 1)
+        return MOE_ERR_INVALID_ARG;
     if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
@@ -163,6 +165,8 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.l2_block_n = tune ? tune->l2_block_n : 0;
     a.group_rows = tune ? tune->group_rows : 0;
     a.cta_group = tune ? tune->cta_group : 0;
+    a.wait_limit_us = tune ? tune->wait_limit_us : 0;
+    a.unmet_dependency = tune ? tune->unmet_dependency : 0;
     a.trace = tune ? static_cast<unsigned long long *>(tune->trace) : nullptr;
     a.counters_zeroed = counters_zeroed;
     a.epoch = next_epoch();

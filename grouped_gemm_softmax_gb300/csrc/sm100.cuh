@@ -20,8 +20,9 @@ enum : unsigned {
     kWhereEpiTmemFull = 5, kWhereDispatch = 6, kWhereGemmOffsets = 7
 };
 
-// Wall-clock limit of any single wait (ns). The longest legitimate wait is a
-// Linear-2 tile waiting for Linear-1 rows, bounded by one whole layer (ms).
+// Default wall-clock limit of any single wait (ns). The longest legitimate
+// wait is a Linear-2 tile waiting for Linear-1 rows, bounded by one whole
+// layer (milliseconds).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer_ns()
@@ -94,10 +95,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait until the phase with the given parity has completed. Gives up (and
-// records a timeout) after kWaitLimitNs, or as soon as this CTA or any CTA of
-// the grid has already given up. Returns false when it gave up.
+// records a timeout) after limit_ns, or as soon as this CTA or any CTA of the
+// grid has already given up. Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *cta_abort,
-                                          unsigned *status, unsigned where, unsigned detail)
+                                          unsigned *status, unsigned where, unsigned detail,
+                                          unsigned long long limit_ns)
 {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
@@ -110,12 +112,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
                 *cta_abort = 1;
                 return false;
             }
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 report_failure(status, kStatusTimeout, where, detail);
                 *cta_abort = 1;
                 return false;
             }
         }
+    }
+}
+
+// Bounded wait that ignores abort requests (used to drain outstanding work
+// before tensor memory is freed). Returns false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
+                                                unsigned long long limit_ns)
+{
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(a, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

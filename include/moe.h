@@ -81,6 +81,10 @@ typedef struct {
                        128-row M-tiles, so each weight tile is reused while hot in L2; 0 = default */
     int cta_group;  /* CTAs per MMA tile: 2 = CTA pairs with 256-row tiles, 1 = single CTAs
                        with 128-row tiles; 0 = default (pairs when T*k/E >= 1024) */
+    int wait_limit_us;    /* limit of every bounded wait in the grouped GEMM; 0 = 2 s */
+    int unmet_dependency; /* failure-detection test only: 1 makes each Linear-2 tile wait for one
+                             more finished Linear-1 tile than exists, so the wait runs out and the
+                             call reports MOE_ERR_TIMEOUT; must be 0 otherwise */
     void *trace;    /* optional device buffer of num_ctas x 16 uint64 per-CTA counters (wait
                        cycles per role, tile counts, start/end times); NULL = off */
 } moe_tuning_t;
