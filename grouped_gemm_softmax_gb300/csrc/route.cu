@@ -14,8 +14,8 @@
 // selection is therefore reproducible bit for bit by any implementation of
 // that sum.
 //
-// Block tile: BT tokens x BE >= E experts, staged through shared memory 32
-// features at a time as fp32 rows (the next chunk is prefetched into registers
+// Block tile: BT tokens x BE >= E experts, staged through shared memory a
+// chunk of features at a time as fp32 rows (the next chunk is prefetched into registers
 // while the current one is used), each thread owning TM tokens x TN experts.
 // Then one warp per token runs k rounds of a shuffle arg-max over the block's
 // logits and writes idx and gates.
@@ -27,7 +27,6 @@
 namespace moe {
 namespace {
 
-constexpr int kBK = 32;  // features per shared-memory chunk
 
 struct RouteParams {
     const uint16_t *x;
@@ -48,7 +47,7 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
 // tb + a + 8i (i < TM) and experts eb + b + 4j (j < TN), so for any fixed i
 // (or j) the warp touches consecutive rows of the shared tiles, which are
 // padded to 36 floats a row: every 16-byte access is bank-conflict free.
-template <int TM, int TN, int WE, int WT>
+template <int TM, int TN, int WE, int WT, int kBK>
 __global__ void __launch_bounds__(32 * WE * WT) route_kernel(const RouteParams p)
 {
     constexpr int NT = 32 * WE * WT;
@@ -229,7 +228,7 @@ __global__ void __launch_bounds__(32 * WE * WT) route_kernel(const RouteParams p
     }
 }
 
-template <int TM, int TN, int WE, int WT>
+template <int TM, int TN, int WE, int WT, int kBK>
 cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
 {
     constexpr int NT = 32 * WE * WT;
@@ -240,14 +239,14 @@ cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
     constexpr size_t smem = stage > logits ? stage : logits;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel<TM, TN, WE, WT>,
+        cudaError_t e = cudaFuncSetAttribute(route_kernel<TM, TN, WE, WT, kBK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
-    route_kernel<TM, TN, WE, WT><<<grid, NT, smem, s>>>(p);
+    route_kernel<TM, TN, WE, WT, kBK><<<grid, NT, smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -257,14 +256,14 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
 {
     if (a.T == 0) return cudaSuccess;
     RouteParams p{a.x, a.wr, a.bias, a.topk_idx, a.topk_gate, a.T, a.d, a.E, a.k};
-    // <TM, TN, WE, WT>: a block covers every expert (BE = 4*WE*TN >= E) and
-    // BT = 8*WT*TM tokens; small token tiles keep the 152 SMs evenly loaded
-    if (a.E > 128) return launch_variant<8, 8, 8, 1>(p, s);  // BT 64, BE 256
-    if (a.E > 64) return launch_variant<2, 8, 4, 2>(p, s);   // BT 32, BE 128
-    if (a.E > 32) return launch_variant<2, 4, 4, 1>(p, s);   // BT 16, BE 64
-    if (a.E > 16) return launch_variant<2, 2, 4, 2>(p, s);   // BT 32, BE 32
-    if (a.E > 8) return launch_variant<2, 1, 4, 2>(p, s);    // BT 32, BE 16
-    return launch_variant<1, 1, 2, 4>(p, s);                 // BT 32, BE 8
+    // a block covers every expert (BE = 4*WE*TN >= E) and BT = 8*WT*TM tokens
+    // <TM, TN, WE, WT, chunk>: measured best per expert count on GB300
+    if (a.E > 128) return launch_variant<8, 8, 8, 1, 32>(p, s);   // BT 64, BE 256
+    if (a.E > 64) return launch_variant<2, 8, 4, 2, 64>(p, s);    // BT 32, BE 128
+    if (a.E > 32) return launch_variant<2, 4, 4, 2, 128>(p, s);   // BT 32, BE 64
+    if (a.E > 16) return launch_variant<2, 2, 4, 2, 128>(p, s);   // BT 32, BE 32
+    if (a.E > 8) return launch_variant<2, 4, 1, 8, 128>(p, s);    // BT 128, BE 16
+    return launch_variant<2, 2, 1, 4, 128>(p, s);                 // BT 64, BE 8
 }
 
 }  // namespace moe
