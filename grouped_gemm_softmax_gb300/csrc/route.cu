@@ -42,6 +42,67 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
     return __uint_as_float(bits16 << 16);
 }
 
+// One warp per token of the block: k rounds of a shuffle arg-max (descending
+// logit, ties to the lower expert index) over the block's logits, then the
+// softmax of the k selected logits in fp32.
+template <int BE, int NW>
+__device__ __forceinline__ void select_topk(const RouteParams &p, const float *lg, long t0, int BT,
+                                            int warp, int lane)
+{
+    for (int r = warp; r < BT; r += NW) {
+        const long t = t0 + r;
+        if (t >= p.T) break;
+        const float *row = lg + r * (BE + 1);
+        constexpr int PER = (BE + 31) / 32;
+        float v[PER];
+        uint32_t avail = 0;  // bit i: expert lane + 32*i not yet selected
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = lane + 32 * i;
+            if (e < p.E) avail |= 1u << i;
+            v[i] = e < p.E ? row[e] : 0.0f;
+        }
+        int sel_e = 0;
+        float sel_v = 0.0f;
+        for (int j = 0; j < p.k; ++j) {
+            float bv = -FLT_MAX;
+            int be = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int e = lane + 32 * i;
+                if (((avail >> i) & 1u) && (be == INT_MAX || v[i] > bv || (v[i] == bv && e < be))) {
+                    bv = v[i];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+            if (lane == j) {
+                sel_e = be;
+                sel_v = bv;
+            }
+        }
+        // softmax over the k selected logits (lane j holds choice j)
+        const float zmax = __shfl_sync(0xffffffffu, sel_v, 0);
+        const float ex = lane < p.k ? expf(sel_v - zmax) : 0.0f;
+        float den = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (lane < p.k) {
+            p.idx[t * p.k + lane] = sel_e;
+            p.gate[t * p.k + lane] = ex / den;
+        }
+    }
+}
+
 // Thread layout: lane = 8 token lanes x 4 expert lanes; warps = WE along
 // experts x WT along tokens. Thread (a, b) of warp (we, wt) owns tokens
 // tb + a + 8i (i < TM) and experts eb + b + 4j (j < TN), so for any fixed i
@@ -174,58 +235,122 @@ __global__ void __launch_bounds__(32 * WE * WT) route_kernel(const RouteParams p
     }
     __syncthreads();
 
-    for (int r = warp; r < BT; r += NW) {
-        const long t = t0 + r;
-        if (t >= p.T) break;
-        const float *row = lg + r * (BE + 1);
-        constexpr int PER = (BE + 31) / 32;
-        float v[PER];
-        uint32_t avail = 0;  // bit i: expert lane + 32*i not yet selected
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = lane + 32 * i;
-            if (e < p.E) avail |= 1u << i;
-            v[i] = e < p.E ? row[e] : 0.0f;
+    select_topk<BE, NW>(p, lg, t0, BT, warp, lane);
+}
+
+// Small expert counts: the FMA work per token is light, so the kernel is bound
+// by how many bytes of x each SM has in flight. This variant streams raw bf16
+// chunks of KB features into a STAGES-deep shared-memory ring with cp.async
+// (16-byte copies, zero-filled past the end) and widens to fp32 at use. Same
+// thread layout and the same ascending-feature accumulation as route_kernel.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src, bool valid)
+{
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int TM, int TN, int WE, int WT, int KB, int STAGES>
+__global__ void __launch_bounds__(32 * WE * WT) route_kernel_async(const RouteParams p)
+{
+    constexpr int NT = 32 * WE * WT;
+    constexpr int BT = WT * 8 * TM;
+    constexpr int BE = WE * 4 * TN;
+    constexpr int NW = NT / 32;
+    constexpr int LD = KB + 8;  // padded row (bf16): rows 4 banks apart
+    constexpr int STAGE = (BT + BE) * LD;  // bf16 per stage
+    constexpr int CPR = KB / 8;            // 16-byte copies per row
+    extern __shared__ __align__(16) uint16_t rsm16[];
+    float *lg = reinterpret_cast<float *>(rsm16);  // [BT][BE + 1] after the K loop
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int a = lane & 7, b = lane >> 3;
+    const int eb = (warp % WE) * 4 * TN, tb = (warp / WE) * 8 * TM;
+    const long t0 = static_cast<long>(blockIdx.x) * BT;
+    const int nchunks = (p.d + KB - 1) / KB;
+
+    auto issue = [&](int chunk) {
+        uint16_t *st = rsm16 + (chunk % STAGES) * STAGE;
+        const int k0 = chunk * KB;
+        for (int v = tid; v < (BT + BE) * CPR; v += NT) {
+            const int r = v / CPR, c8 = (v % CPR) * 8;
+            const bool is_x = r < BT;
+            const long row = is_x ? t0 + r : static_cast<long>(r - BT);
+            const bool ok = k0 + c8 < p.d && (is_x ? row < p.T : row < p.E);
+            const uint16_t *src = is_x ? p.x + (ok ? row * p.d + k0 + c8 : 0)
+                                       : p.wr + (ok ? row * p.d + k0 + c8 : 0);
+            cp_async_16(st + r * LD + c8, src, ok);
         }
-        int sel_e = 0;
-        float sel_v = 0.0f;
-        for (int j = 0; j < p.k; ++j) {
-            float bv = -FLT_MAX;
-            int be = INT_MAX;
+    };
+
+    float acc[TM][TN];
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int e = lane + 32 * i;
-                if (((avail >> i) & 1u) && (be == INT_MAX || v[i] > bv || (v[i] == bv && e < be))) {
-                    bv = v[i];
-                    be = e;
-                }
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+    for (int c = 0; c < STAGES - 1; ++c) {
+        if (c < nchunks) issue(c);
+        cp_async_commit();
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        if (c + STAGES - 1 < nchunks) issue(c + STAGES - 1);
+        cp_async_commit();
+        const uint16_t *xs = rsm16 + (c % STAGES) * STAGE;
+        const uint16_t *ws = xs + BT * LD;
+#pragma unroll 4
+        for (int kk = 0; kk < KB; kk += 4) {
+            float xv[TM][4], wv[TN][4];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const uint2 q = *reinterpret_cast<const uint2 *>(xs + (tb + a + 8 * i) * LD + kk);
+                xv[i][0] = bf16_bits_to_f32(q.x & 0xFFFFu);
+                xv[i][1] = bf16_bits_to_f32(q.x >> 16);
+                xv[i][2] = bf16_bits_to_f32(q.y & 0xFFFFu);
+                xv[i][3] = bf16_bits_to_f32(q.y >> 16);
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
+            for (int j = 0; j < TN; ++j) {
+                const uint2 q = *reinterpret_cast<const uint2 *>(ws + (eb + b + 4 * j) * LD + kk);
+                wv[j][0] = bf16_bits_to_f32(q.x & 0xFFFFu);
+                wv[j][1] = bf16_bits_to_f32(q.x >> 16);
+                wv[j][2] = bf16_bits_to_f32(q.y & 0xFFFFu);
+                wv[j][3] = bf16_bits_to_f32(q.y >> 16);
             }
-            if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
-            if (lane == j) {
-                sel_e = be;
-                sel_v = bv;
-            }
-        }
-        // softmax over the k selected logits (lane j holds choice j)
-        const float zmax = __shfl_sync(0xffffffffu, sel_v, 0);
-        const float ex = lane < p.k ? expf(sel_v - zmax) : 0.0f;
-        float den = ex;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        if (lane < p.k) {
-            p.idx[t * p.k + lane] = sel_e;
-            p.gate[t * p.k + lane] = ex / den;
+            for (int f = 0; f < 4; ++f)  // ascending feature order
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i][f], wv[j][f], acc[i][j]);
         }
     }
+    cp_async_wait<0>();
+    __syncthreads();
+
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int e = eb + b + 4 * j;
+            float z = acc[i][j];
+            if (p.bias != nullptr && e < p.E) z = z + p.bias[e];
+            lg[(tb + a + 8 * i) * (BE + 1) + e] = z;
+        }
+    }
+    __syncthreads();
+    select_topk<BE, NW>(p, lg, t0, BT, warp, lane);
 }
 
 template <int TM, int TN, int WE, int WT, int kBK>
@@ -250,6 +375,28 @@ cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
     return cudaGetLastError();
 }
 
+template <int TM, int TN, int WE, int WT, int KB, int STAGES>
+cudaError_t launch_variant_async(const RouteParams &p, cudaStream_t s)
+{
+    constexpr int NT = 32 * WE * WT;
+    constexpr int BT = WT * 8 * TM;
+    constexpr int BE = WE * 4 * TN;
+    constexpr size_t stage = sizeof(uint16_t) * STAGES * (BT + BE) * (KB + 8);
+    constexpr size_t logits = sizeof(float) * BT * (BE + 1);
+    constexpr size_t smem = stage > logits ? stage : logits;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(route_kernel_async<TM, TN, WE, WT, KB, STAGES>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
+    route_kernel_async<TM, TN, WE, WT, KB, STAGES><<<grid, NT, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
@@ -260,10 +407,10 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     // <TM, TN, WE, WT, chunk>: measured best per expert count on GB300
     if (a.E > 128) return launch_variant<8, 8, 8, 1, 32>(p, s);   // BT 64, BE 256
     if (a.E > 64) return launch_variant<2, 8, 4, 2, 64>(p, s);    // BT 32, BE 128
-    if (a.E > 32) return launch_variant<2, 4, 4, 2, 128>(p, s);   // BT 32, BE 64
-    if (a.E > 16) return launch_variant<2, 2, 4, 2, 128>(p, s);   // BT 32, BE 32
-    if (a.E > 8) return launch_variant<2, 4, 1, 8, 128>(p, s);    // BT 128, BE 16
-    return launch_variant<2, 2, 1, 4, 128>(p, s);                 // BT 64, BE 8
+    if (a.E > 32) return launch_variant_async<2, 4, 4, 1, 128, 4>(p, s);  // BT 16, BE 64
+    if (a.E > 16) return launch_variant<2, 2, 4, 2, 128>(p, s);           // BT 32, BE 32
+    if (a.E > 8) return launch_variant<2, 4, 1, 8, 128>(p, s);            // BT 128, BE 16
+    return launch_variant_async<1, 1, 2, 4, 128, 4>(p, s);                // BT 32, BE 8
 }
 
 }  // namespace moe
