@@ -15,7 +15,11 @@ from gpu_helpers import assert_close, bits, need_gpu, to_f64
 
 pytestmark = pytest.mark.gpu
 
-WHERE_PRODUCER_DEPENDENCY = 2
+# where the timeout is recorded: the producer's wait for the Linear-1 rows, or
+# a wait that starves behind it (the MMA thread's wait for the next loaded
+# stage, the epilogue's wait for the next accumulator), whichever limit runs
+# out first
+WHERE_STARVED = {2, 3, 5}
 
 
 def _case(counts, d, F):
@@ -44,7 +48,7 @@ def test_unmet_dependency_times_out_and_the_context_survives(cg):
     elapsed = time.time() - t0
     assert st == moe.MOE_ERR_TIMEOUT
     where, block, detail = moe.last_device_detail()
-    assert where == WHERE_PRODUCER_DEPENDENCY
+    assert where in WHERE_STARVED
     assert elapsed < 10.0
     assert moe.last_device_status(ws) == moe.MOE_OK  # reading it cleared it
 
