@@ -54,7 +54,8 @@ class _CTuning(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int), ("lead_rows", ctypes.c_int), ("num_ctas", ctypes.c_int),
                 ("l2_block_n", ctypes.c_int), ("group_rows", ctypes.c_int), ("cta_group", ctypes.c_int),
                 ("wait_limit_us", ctypes.c_int), ("unmet_dependency", ctypes.c_int),
-                ("trace", ctypes.c_void_p)]
+                ("trace", ctypes.c_void_p), ("tile_trace", ctypes.c_void_p),
+                ("tile_trace_cap", ctypes.c_int), ("reserved2", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -75,6 +76,9 @@ class Shape:
 
 
 TRACE_WORDS = 16  # per-CTA uint64 counters written when Tuning.trace is given
+TILE_TRACE_WORDS = 8  # per-tile record words written when Tuning.tile_trace is given
+TILE_TRACE_FIELDS = ("tile", "prod_start", "prod_dep_wait", "mma_start", "mma_last_issue",
+                     "mma_stage_wait", "epi_start", "epi_end")
 TRACE_FIELDS = ("prod_wait_empty", "prod_wait_rows", "prod_cycles", "mma_wait_full", "mma_wait_tmem",
                 "mma_cycles", "epi_wait_full", "epi_work", "epi_wait_stores", "epi_cycles", "l1_tiles",
                 "l2_tiles", "t_start_ns", "t_end_ns", "unused14", "unused15")
@@ -91,11 +95,15 @@ class Tuning:
     wait_limit_us: int = 0
     unmet_dependency: int = 0
     trace: object = None  # optional torch int64 CUDA tensor of >= num_ctas * TRACE_WORDS entries
+    tile_trace: object = None  # optional torch int64 CUDA tensor, num_ctas * cap * TILE_TRACE_WORDS
+    tile_trace_cap: int = 0
 
     def c(self) -> _CTuning:
         tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
+        tt = None if self.tile_trace is None else _ptr(self.tile_trace, torch.int64, None, "tile_trace")
         return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
-                        self.cta_group, self.wait_limit_us, self.unmet_dependency, tr)
+                        self.cta_group, self.wait_limit_us, self.unmet_dependency, tr, tt,
+                        self.tile_trace_cap, 0)
 
 
 _lib = None

@@ -58,6 +58,12 @@ constexpr uint32_t kAccCols = 256;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kTraceWords = 16;  // per-CTA counters when tracing is on
+// per-tile timeline record (clock64 of the CTA's SM):
+// 0 kind | row << 2 | n << 34, 1 producer start (after its dependency wait),
+// 2 producer dependency-wait cycles, 3 MMA start (accumulator free), 4 MMA last
+// issue, 5 MMA stage-wait cycles, 6 epilogue start (accumulator ready),
+// 7 epilogue stores done
+constexpr int kTileTraceWords = 8;
 
 template <int CG>
 struct Cfg {
@@ -81,6 +87,8 @@ struct GemmParams {
     unsigned long long wait_ns;  // limit of every bounded wait
     unsigned epoch;
     unsigned long long *trace;
+    unsigned long long *tile_trace;  // optional per-tile timeline: [CTA][cap][kTileTraceWords]
+    int tile_trace_cap;
 };
 
 struct SmemCtl {
@@ -96,7 +104,7 @@ struct SmemCtl {
     int offs[kMaxExperts + 1];       // expert row offsets (copy of expert_offsets)
     int row_start[kMaxExperts + 1];  // first scheduler row of each expert
     int wave_row[kMaxExperts + 1];   // wave w spans scheduler rows [wave_row[w], wave_row[w+1])
-    long wave_tile[kMaxExperts + 1]; // first global tile index of wave w
+    int wave_tile[kMaxExperts + 1];  // first global tile index of wave w
 };
 
 // epilogue transpose buffer: per epilogue warp, 32 rows x 64 bf16 (128 B a row)
@@ -111,54 +119,53 @@ constexpr size_t smem_bytes()
 
 struct Tile {
     int kind;  // 0 = Linear-1, 1 = Linear-2, -1 = no more tiles
-    int row;
-    int n;
+    int row;   // scheduler row
+    int n;     // N-tile
+    int e;     // expert owning the row
 };
-
-// expert owning scheduler row `row` (the last e with row_start[e] <= row)
-__device__ __forceinline__ int row_expert(const SmemCtl &c, int E, int row)
-{
-    int lo = 0, hi = E;  // row_start[lo] <= row < row_start[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (c.row_start[mid] <= row) lo = mid;
-        else hi = mid;
-    }
-    return lo;
-}
 
 // Position k of a tile stream (Pn N-tiles per scheduler row) -> (row, n). Tiles
 // of one expert occupy positions [row_start[e]*Pn, row_start[e+1]*Pn); inside
 // the expert they run over groups of GM consecutive rows, N-tile-major within a
 // group, so a weight tile is reused by the group's M-tiles back to back. Every
-// tile of row p sits below position (p + GM) * Pn.
-__device__ __forceinline__ Tile stream_tile(const SmemCtl &c, int E, long k, int Pn, int GM, int kind)
-{
-    Tile t;
-    t.kind = kind;
-    const int e = row_expert(c, E, static_cast<int>(k / Pn));
-    const int r0 = c.row_start[e];
-    const long local = k - static_cast<long>(r0) * Pn;
-    const long per_group = static_cast<long>(GM) * Pn;
-    const int j = static_cast<int>(local / per_group);
-    const int gs = min(GM, c.row_start[e + 1] - r0 - j * GM);
-    const int i = static_cast<int>(local - j * per_group);
-    t.n = i / gs;
-    t.row = r0 + j * GM + i % gs;
-    return t;
-}
+// tile of row p sits below position (p + GM) * Pn. A CTA only ever asks for
+// increasing positions of a stream, so the expert is found by advancing a
+// cursor (32-bit arithmetic: this runs on the MMA thread between tiles).
+struct StreamCursor {
+    int e = 0;
+
+    __device__ Tile at(const SmemCtl &c, int E, int k, int Pn, int GM, int kind)
+    {
+        while (e + 1 < E && c.row_start[e + 1] * Pn <= k) ++e;
+        Tile t;
+        t.kind = kind;
+        t.e = e;
+        const int r0 = c.row_start[e];
+        const int local = k - r0 * Pn;
+        const int per_group = GM * Pn;
+        const int j = local / per_group;
+        const int gs = min(GM, c.row_start[e + 1] - r0 - j * GM);
+        const int i = local - j * per_group;
+        t.n = i / gs;
+        t.row = r0 + j * GM + i % gs;
+        return t;
+    }
+};
 
 // Every role of a CTA runs its own copy of this deterministic walk, so they all
 // see the same tile sequence without communicating.
 struct Scheduler {
-    long k1, k2, tot1, tot2;
-    long gi;
+    int k1, k2, tot1, tot2;
+    int gi;
     int w;
     int P1, P2, G, D, GM, mode;
+    StreamCursor s1, s2;
+    Tile t2;         // decoded Linear-2 tile at k2 (interleaved mode)
+    bool t2_valid;
 
     __device__ Scheduler(const SmemCtl &c, const GemmParams &p)
     {
-        const long P = c.row_start[p.E];
+        const int P = c.row_start[p.E];
         P1 = p.P1;
         P2 = p.P2;
         G = gridDim.x / p.cg;
@@ -170,6 +177,7 @@ struct Scheduler {
         tot2 = P * P2;
         gi = blockIdx.x / p.cg;
         w = 0;
+        t2_valid = false;
     }
 
     __device__ Tile next(const SmemCtl &c, int E)
@@ -182,15 +190,19 @@ struct Scheduler {
                 t.kind = -1;
                 return t;
             }
-            const long p1 = (k1 < tot1) ? k1 / P1 : LONG_MAX / 2;
+            const int p1 = (k1 < tot1) ? k1 / P1 : INT_MAX / 2;
             if (k2 < tot2) {
-                const Tile t2 = stream_tile(c, E, k2, P2, GM, 1);
+                if (!t2_valid) {
+                    t2 = s2.at(c, E, k2, P2, GM, 1);
+                    t2_valid = true;
+                }
                 if (t2.row + D <= p1) {
                     k2 += G;
+                    t2_valid = false;
                     return t2;
                 }
             }
-            t = stream_tile(c, E, k1, P1, GM, 0);
+            t = s1.at(c, E, k1, P1, GM, 0);
             k1 += G;
             return t;
         }
@@ -200,12 +212,12 @@ struct Scheduler {
             return t;
         }
         while (gi >= c.wave_tile[w + 1]) ++w;
-        const long j = gi - c.wave_tile[w];
+        const int j = gi - c.wave_tile[w];
         const int r0 = c.wave_row[w];
-        const long nr = c.wave_row[w + 1] - r0;
+        const int nr = c.wave_row[w + 1] - r0;
         gi += G;
-        if (j < nr * P1) return stream_tile(c, E, static_cast<long>(r0) * P1 + j, P1, GM, 0);
-        return stream_tile(c, E, static_cast<long>(r0) * P2 + (j - nr * P1), P2, GM, 1);
+        if (j < nr * P1) return s1.at(c, E, r0 * P1 + j, P1, GM, 0);
+        return s2.at(c, E, r0 * P2 + (j - nr * P1), P2, GM, 1);
     }
 };
 
@@ -339,14 +351,14 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             // expert waves for the comparison schedule: consecutive experts until
             // the wave's Linear-1 tiles fill the grid once
             int nw = 0;
-            long tiles = 0;
+            int tiles = 0;
             c.wave_row[0] = 0;
             c.wave_tile[0] = 0;
             int wr = 0;
             for (int e = 0; e < E; ++e) {
                 const int r1 = c.row_start[e + 1];
                 if (static_cast<long>(r1 - wr) * p.P1 >= gridDim.x / CG || e == E - 1) {
-                    tiles += static_cast<long>(r1 - wr) * (p.P1 + p.P2);
+                    tiles += (r1 - wr) * (p.P1 + p.P2);
                     ++nw;
                     c.wave_row[nw] = r1;
                     c.wave_tile[nw] = tiles;
@@ -371,10 +383,15 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             uint32_t ph = 0;
             bool ok = true;
             unsigned long long w_empty = 0, w_rows = 0, t0 = tr ? clock64() : 0;
-            while (ok) {
+            for (int tl = 0; ok; ++tl) {
                 const Tile t = sch.next(c, E);
                 if (t.kind < 0) break;
-                const int e = row_expert(c, E, t.row);
+                unsigned long long *rec =
+                    (p.tile_trace && tl < p.tile_trace_cap)
+                        ? p.tile_trace + (static_cast<long>(blockIdx.x) * p.tile_trace_cap + tl) * kTileTraceWords
+                        : nullptr;
+                unsigned long long dep0 = rec ? clock64() : 0;
+                const int e = t.e;
                 // this CTA's 128 rows of the scheduler row
                 const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows +
                                  static_cast<int>(rank) * kBlockM;
@@ -387,6 +404,14 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         break;
                     if (tr) w_rows += clock64() - tw;
                     fence_proxy_async_global();
+                }
+                if (rec) {
+                    const unsigned long long now = clock64();
+                    rec[0] = static_cast<unsigned long long>(t.kind) |
+                             (static_cast<unsigned long long>(t.row) << 2) |
+                             (static_cast<unsigned long long>(t.n) << 34);
+                    rec[1] = now;
+                    rec[2] = t.kind == 1 ? now - dep0 : 0;
                 }
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
                 // bytes of one stage summed over the CTAs of the pair
@@ -442,8 +467,11 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             const uint32_t idesc2 = idesc_bf16_f32(kTileRows, p.N2);
             bool ok = true;
             unsigned long long w_full = 0, w_tmem = 0, t0 = tr ? clock64() : 0;
+            // the next tile is worked out while the current tile's first MMAs
+            // run, so the tensor pipe does not idle between tiles
+            Tile t_next = sch.next(c, E);
             for (int tl = 0; ok; ++tl) {
-                const Tile t = sch.next(c, E);
+                const Tile t = t_next;
                 if (t.kind < 0) break;
                 const int b = tl & 1;
                 const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
@@ -452,18 +480,28 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                                static_cast<unsigned>(tl), p.wait_ns))
                     break;
                 if (tr) w_tmem += clock64() - tw;
+                unsigned long long *rec =
+                    (p.tile_trace && tl < p.tile_trace_cap)
+                        ? p.tile_trace + (static_cast<long>(blockIdx.x) * p.tile_trace_cap + tl) * kTileTraceWords
+                        : nullptr;
+                unsigned long long tile_wait = 0;
+                if (rec) rec[3] = clock64();
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b) * kAccCols;
                 const uint32_t idesc = t.kind == 0 ? idesc1 : idesc2;
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    tw = tr ? clock64() : 0;
+                    tw = (tr || rec) ? clock64() : 0;
                     if (!mbar_wait(&c.full[s], ph, abort_flag, p.status, kWhereMmaFull,
                                    static_cast<unsigned>(s), p.wait_ns)) {
                         ok = false;
                         break;
                     }
-                    if (tr) w_full += clock64() - tw;
+                    if (tr || rec) {
+                        const unsigned long long dw = clock64() - tw;
+                        w_full += dw;
+                        tile_wait += dw;
+                    }
                     tc_fence_after();
                     const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + s * kATileBytes));
                     const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + s * kBTileBytes));
@@ -474,10 +512,15 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                                         (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit<CG>(&c.empty[s]);
+                    if (kb == 0) t_next = sch.next(c, E);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
                     }
+                }
+                if (rec) {
+                    rec[4] = clock64();
+                    rec[5] = tile_wait;
                 }
                 if (ok) mma_commit<CG>(&c.tfull[b]);
             }
@@ -510,6 +553,11 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             const bool ready = mbar_wait(&c.tfull[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
                                          static_cast<unsigned>(tl), p.wait_ns);
             if (!__all_sync(0xffffffffu, ready)) break;
+            unsigned long long *rec =
+                (publisher && p.tile_trace && tl < p.tile_trace_cap)
+                    ? p.tile_trace + (static_cast<long>(blockIdx.x) * p.tile_trace_cap + tl) * kTileTraceWords
+                    : nullptr;
+            if (rec) rec[6] = clock64();
             if (tr) {
                 const unsigned long long now = clock64();
                 w_full += now - tw;
@@ -518,7 +566,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 else ++n2;
             }
             tc_fence_after();
-            const int e = row_expert(c, E, t.row);
+            const int e = t.e;
             const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows +
                              static_cast<int>(rank) * kBlockM;
             const int valid_rows = min(kBlockM, c.offs[e + 1] - row0);  // may be <= 0
@@ -587,6 +635,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                                               kWhereEpiTmemFull, 0x80000000u | static_cast<unsigned>(tl),
                                               p.wait_ns);
                 if (tr) w_stores += clock64() - tw;
+                if (rec) rec[7] = clock64();
                 if (stored) {
                     __threadfence();
                     if (t.kind == 0)
@@ -768,6 +817,8 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.schedule = a.schedule;
     p.epoch = a.epoch;
     p.trace = a.trace;
+    p.tile_trace = a.tile_trace;
+    p.tile_trace_cap = a.tile_trace_cap;
     p.wait_ns = a.wait_limit_us > 0 ? 1000ull * static_cast<unsigned long long>(a.wait_limit_us)
                                     : kWaitLimitNs;
     p.unmet_dependency = a.unmet_dependency > 0 ? 1 : 0;

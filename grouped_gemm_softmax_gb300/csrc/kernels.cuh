@@ -56,6 +56,8 @@ struct FfnArgs {
     int schedule, lead, num_ctas, l2_block_n, group_rows, cta_group;
     int wait_limit_us, unmet_dependency;
     unsigned long long *trace;  // optional per-CTA counters (16 per CTA)
+    unsigned long long *tile_trace;  // optional per-tile timeline (8 words per tile)
+    int tile_trace_cap;              // tiles recorded per CTA
     bool counters_zeroed;    // l1_done already cleared by an earlier kernel on the stream
     unsigned epoch;
 };

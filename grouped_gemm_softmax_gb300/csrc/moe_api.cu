@@ -134,6 +134,9 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->group_rows < 0 || t->cta_group < 0 || t->cta_group > 2) return MOE_ERR_INVALID_ARG;
     if (t->wait_limit_us < 0 || t->unmet_dependency < 0 || t->unmet_dependency > 1)
         return MOE_ERR_INVALID_ARG;
+    if (t->tile_trace && (t->tile_trace_cap <= 0 || (reinterpret_cast<uintptr_t>(t->tile_trace) & 7u)))
+        return MOE_ERR_INVALID_ARG;
+    if (t->reserved2 != 0) return MOE_ERR_INVALID_ARG;
     if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
@@ -168,6 +171,8 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.wait_limit_us = tune ? tune->wait_limit_us : 0;
     a.unmet_dependency = tune ? tune->unmet_dependency : 0;
     a.trace = tune ? static_cast<unsigned long long *>(tune->trace) : nullptr;
+    a.tile_trace = tune ? static_cast<unsigned long long *>(tune->tile_trace) : nullptr;
+    a.tile_trace_cap = tune ? tune->tile_trace_cap : 0;
     a.counters_zeroed = counters_zeroed;
     a.epoch = next_epoch();
     if (moe::encode_tiled_fn() == nullptr) return MOE_ERR_CUDA;

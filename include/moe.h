@@ -87,6 +87,12 @@ typedef struct {
                              call reports MOE_ERR_TIMEOUT; must be 0 otherwise */
     void *trace;    /* optional device buffer of num_ctas x 16 uint64 per-CTA counters (wait
                        cycles per role, tile counts, start/end times); NULL = off */
+    void *tile_trace;   /* optional per-tile timeline: num_ctas x tile_trace_cap x 8 uint64
+                           (SM clock stamps: tile id, producer start and dependency wait,
+                           MMA start / last issue / stage-wait cycles, epilogue start / end);
+                           NULL = off */
+    int tile_trace_cap; /* tiles recorded per CTA (later tiles are not recorded) */
+    int reserved2;      /* must be 0 */
 } moe_tuning_t;
 
 /* Human-readable name of a status code. Never NULL. */
