@@ -8,9 +8,10 @@
 //   2. scan    one block: per expert, exclusive scan over chunks, then over
 //              experts -> expert_counts, expert_offsets, and each chunk's
 //              first row per expert; also clears the grouped GEMM's counters
-//   3. rank    one block per chunk: warp 0 walks the chunk's slots in order,
-//              32 at a time, ranking equal experts with __match_any_sync, and
-//              writes row_of_slot / slot_of_row
+//   3. rank    one block per chunk: each warp takes a contiguous slice of the
+//              chunk's slots; per-warp counts and a prefix over warps give each
+//              warp its bases; it then ranks equal experts 32 slots at a time
+//              with __match_any_sync and writes row_of_slot / slot_of_row
 //   4. copy    one warp per token: x[t] read once with 16-byte loads and
 //              written to its k destination rows
 #include "kernels.cuh"
@@ -88,45 +89,73 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t *chunk_base, int
     for (long i = threadIdx.x; i < zero_count; i += kThreads) zero_words[i] = 0u;
 }
 
+// Each warp of the block owns a contiguous slice of the staged slots. Pass 1:
+// per-warp, per-expert counts. Then each expert's base for warp w is the
+// chunk's base plus the counts of warps 0..w-1 (slot order is preserved).
+// Pass 2: each warp ranks its slice 32 slots at a time (__match_any_sync),
+// in order, from its own bases.
 __global__ void __launch_bounds__(kThreads) rank_kernel(const int32_t *__restrict__ idx, int T, int k,
                                                         int E, int C,
                                                         const int32_t *__restrict__ chunk_base,
                                                         int32_t *row_of_slot, int32_t *slot_of_row)
 {
-    __shared__ int cur[kMaxExperts];
+    constexpr int NW = kThreads / 32;
+    __shared__ int cur[kMaxExperts];            // running base per expert across batches
+    __shared__ int wcnt[NW][kMaxExperts];       // per-warp counts, then per-warp bases
     __shared__ int sidx[kRankBatch];
     for (int e = threadIdx.x; e < E; e += kThreads)
         cur[e] = chunk_base[static_cast<long>(blockIdx.x) * E + e];
     const long s0 = static_cast<long>(blockIdx.x) * C * k;
     const long s1 = min(static_cast<long>(T), static_cast<long>(blockIdx.x + 1) * C) * k;
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
     for (long b0 = s0; b0 < s1; b0 += kRankBatch) {
         const int nb = static_cast<int>(min(static_cast<long>(kRankBatch), s1 - b0));
         __syncthreads();
         for (int i = threadIdx.x; i < nb; i += kThreads) sidx[i] = idx[b0 + i];
+        for (int i = threadIdx.x; i < NW * E; i += kThreads) wcnt[i / E][i % E] = 0;
         __syncthreads();
-        if (threadIdx.x < 32) {
-            const unsigned lt = (1u << lane) - 1u;
-            for (int i0 = 0; i0 < nb; i0 += 32) {
-                const int i = i0 + lane;
-                const int e0 = i < nb ? sidx[i] : -1;
-                const bool in_range = e0 >= 0 && e0 < E;
-                const bool valid = i < nb && in_range;
-                const int e = valid ? e0 : -1;
-                if (i < nb && !in_range) row_of_slot[b0 + i] = -1;
-                const unsigned peers = __match_any_sync(0xffffffffu, e);
-                const int rank = __popc(peers & lt);
-                const int base = valid ? cur[e] : 0;
-                __syncwarp();
-                if (valid) {
-                    const int row = base + rank;
-                    const long s = b0 + i;
-                    row_of_slot[s] = row;
-                    slot_of_row[row] = static_cast<int32_t>(s);
-                    if (rank == 0) cur[e] = base + __popc(peers);
-                }
-                __syncwarp();
+        // this warp's slice of the batch, in 32-slot steps
+        const int per = (nb + NW - 1) / NW;
+        const int lo = min(nb, warp * per), hi = min(nb, lo + per);
+        for (int i0 = lo; i0 < hi; i0 += 32) {
+            const int i = i0 + lane;
+            const int e0 = i < hi ? sidx[i] : -1;
+            const int e = (e0 >= 0 && e0 < E) ? e0 : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && __popc(peers & lt) == 0) wcnt[warp][e] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        // exclusive prefix over warps, per expert; advance the running base
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            int run = cur[e];
+            for (int w = 0; w < NW; ++w) {
+                const int c = wcnt[w][e];
+                wcnt[w][e] = run;
+                run += c;
             }
+            cur[e] = run;
+        }
+        __syncthreads();
+        for (int i0 = lo; i0 < hi; i0 += 32) {
+            const int i = i0 + lane;
+            const int e0 = i < hi ? sidx[i] : -1;
+            const bool in_range = e0 >= 0 && e0 < E;
+            const int e = in_range ? e0 : -1;
+            if (i < hi && !in_range) row_of_slot[b0 + i] = -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & lt);
+            const int base = e >= 0 ? wcnt[warp][e] : 0;
+            __syncwarp();
+            if (e >= 0) {
+                const int row = base + rank;
+                const long sl = b0 + i;
+                row_of_slot[sl] = row;
+                slot_of_row[row] = static_cast<int32_t>(sl);
+                if (rank == 0) wcnt[warp][e] = base + __popc(peers);
+            }
+            __syncwarp();
         }
     }
 }
