@@ -17,6 +17,7 @@ path to run).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -53,7 +54,10 @@ def parse_args():
     ap.add_argument("--lead", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--stage", choices=["route"], default=None,
+    ap.add_argument("--timeline", action="store_true",
+                    help="after the timed region, run one traced grouped GEMM and add its "
+                         "per-tile timeline summary to the line")
+    ap.add_argument("--stage", choices=["route", "dispatch", "combine"], default=None,
                     help="time one entry point alone (for profiling) instead of the layer")
     return ap.parse_args()
 
@@ -235,6 +239,62 @@ def traffic_record(cfg_name):
     return rec.get("dram_bytes_per_launch")
 
 
+def timeline_summary(moe, cfg, shape, inp, ws, tuning, dev):
+    """One extra grouped-GEMM launch, outside the timed region, with the per-tile
+    timeline switched on. Cycle counts are each SM's own clock64; only
+    per-CTA differences are used. Summarises how much of each MMA issuer's
+    span went to issuing tiles, the stage (operand) waits inside tiles, the
+    gaps between consecutive tiles and the Linear-2 producers' waits for
+    Linear-1 rows."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cap = int((((cfg.R + 127) // 128 + cfg.E) * ((cfg.F + cfg.d) // 64)) // sms) + 64
+    words = moe.TILE_TRACE_WORDS
+    tt = torch.zeros(sms * cap * words, dtype=torch.int64, device=dev)
+    tr = torch.zeros(sms * moe.TRACE_WORDS, dtype=torch.int64, device=dev)
+    xp = moe.ws_view(ws, shape, moe.WS.X_PERM, torch.bfloat16, (cfg.R, cfg.d))
+    off = moe.ws_view(ws, shape, moe.WS.OFFSETS, torch.int32, (cfg.E + 1,))
+    y = moe.ws_view(ws, shape, moe.WS.Y_PERM, torch.bfloat16, (cfg.R, cfg.d))
+    traced = dataclasses.replace(tuning, trace=tr, tile_trace=tt, tile_trace_cap=cap)
+    moe.expert_ffn(shape, xp, off, inp.w1, inp.w3, inp.w2, y, ws, tuning=traced)
+    torch.cuda.synchronize(dev)
+    st = moe.last_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} {moe.last_device_detail()}")
+    rec = tt.view(sms, cap, words).cpu().numpy().astype(np.int64)
+    ctr = tr.view(sms, moe.TRACE_WORDS).cpu().numpy().astype(np.int64)
+    kind = rec[:, :, 0] & 3
+    issued = (rec[:, :, 3] > 0) & (rec[:, :, 4] > 0)
+    busy = span = wait = 0
+    gaps = []
+    for c in range(sms):
+        v = issued[c]
+        if not v.any():
+            continue
+        st_, en = rec[c, v, 3], rec[c, v, 4]
+        busy += int((en - st_).sum())
+        span += int(en.max() - st_.min())
+        wait += int(rec[c, v, 5].sum())
+        if len(st_) > 1:
+            gaps.append(st_[1:] - en[:-1])
+    g = np.concatenate(gaps) if gaps else np.zeros(1, np.int64)
+    produced = rec[:, :, 1] > 0
+    l2 = produced & (kind == 1)
+    t0 = ctr[:, 12][ctr[:, 12] > 0]
+    t1 = ctr[:, 13][ctr[:, 13] > 0]
+    return {
+        "tiles_l1": int((issued & (kind == 0)).sum()), "tiles_l2": int((issued & (kind == 1)).sum()),
+        "issuing_ctas": int(issued.any(1).sum()),
+        "mma_issue_busy_frac": busy / max(span, 1),
+        "stage_wait_frac_of_issue": wait / max(busy, 1),
+        "gap_between_tiles_cycles_median": float(np.median(g)),
+        "gap_between_tiles_cycles_p90": float(np.percentile(g, 90)),
+        "l2_dependency_wait_cycles_mean": float(rec[:, :, 2][l2].mean()) if l2.any() else 0.0,
+        "l2_tiles_that_waited_frac": float((rec[:, :, 2][l2] > 2000).mean()) if l2.any() else 0.0,
+        "traced_kernel_us": float((t1.max() - t0.min()) / 1e3) if len(t0) and len(t1) else None,
+        "truncated": bool((rec[:, -1, 1] > 0).any()),
+    }
+
+
 def run_ours(args, cfg):
     import grouped_gemm_softmax_gb300 as moe
     from grouped_gemm_softmax_gb300 import build as moe_build
@@ -377,14 +437,33 @@ def run_ours(args, cfg):
         "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks,
         "wall_s_timed": t_wall,
     }
+    if args.lead:
+        line["config"]["lead_rows"] = args.lead
+    if args.timeline:
+        line["timeline"] = timeline_summary(moe, cfg, shape, inp, ws, tuning, dev)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
 
 
+def stage_bytes(cfg, stage):
+    """Algorithmic HBM bytes of one call of a memory-bound entry point: every
+    input read once and every output written once (x read once by dispatch,
+    although each token row is copied k times)."""
+    T, d, E, k, R = cfg.T, cfg.d, cfg.E, cfg.k, cfg.R
+    if stage == "route":
+        return 2.0 * T * d + 2.0 * E * d + 4.0 * E + 8.0 * T * k
+    if stage == "dispatch":
+        return 4.0 * R + 2.0 * T * d + 2.0 * R * d + 8.0 * R + 8.0 * E
+    return 2.0 * R * d + 8.0 * R + 2.0 * T * d  # combine
+
+
 def run_stage(args, cfg):
-    """Time moe_route alone on the config's x and router weights (no expert
-    weights are generated): one JSON line with the stage's mean time."""
+    """Time one entry point alone on the config's inputs (no expert weights are
+    generated): one JSON line with the stage's mean time. dispatch runs on the
+    router's own indices; combine takes the dispatched token rows as its expert
+    outputs (its work does not depend on their values), the router's gates and
+    the dispatch's row map."""
     import grouped_gemm_softmax_gb300 as moe
     from grouped_gemm_softmax_gb300 import build as moe_build
 
@@ -393,23 +472,43 @@ def run_stage(args, cfg):
     dev = torch.device("cuda", 0)
     shape = moe.Shape(T=cfg.T, d=cfg.d, E=cfg.E, top_k=cfg.k, ffn=cfg.F, num_segments=cfg.S)
     inp = synth.make_inputs(cfg, seed=0, device=dev, weights=False)
-    idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx = torch.empty(cfg.T, cfg.k, **i32)
     gate = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+    moe.route(shape, inp.x, inp.wr, inp.bias, idx, gate)
+    if args.stage != "route":
+        counts, offsets = torch.empty(cfg.E, **i32), torch.empty(cfg.E + 1, **i32)
+        ros, sor = torch.empty(cfg.R, **i32), torch.empty(cfg.R, **i32)
+        ws = moe.alloc_workspace(shape, dev)
+        xp = moe.ws_view(ws, shape, moe.WS.X_PERM, torch.bfloat16, (cfg.R, cfg.d))
+        moe.dispatch(shape, inp.x, idx, counts, offsets, ros, sor, xp, ws)
+    if args.stage == "combine":
+        y = xp  # the token rows stand in for the expert outputs
+        segs = [torch.empty(cfg.T // cfg.S, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
+    calls = {
+        "route": lambda: moe.route(shape, inp.x, inp.wr, inp.bias, idx, gate),
+        "dispatch": lambda: moe.dispatch(shape, inp.x, idx, counts, offsets, ros, sor, xp, ws),
+        "combine": lambda: moe.combine(shape, y, gate, ros, segs),
+    }
+    call = calls[args.stage]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        moe.route(shape, inp.x, inp.wr, inp.bias, idx, gate)
+        call()
         b.record()
         if i >= args.warmup:
             ev.append((a, b))
     torch.cuda.synchronize()
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    print(json.dumps({"stage": args.stage, "config": workload_config(cfg, "n/a"), "ms": ms,
-                      "fp32_tflops": 2.0 * cfg.T * cfg.d * cfg.E / (ms / 1000.0) / 1e12,
-                      "steps": args.steps}), flush=True)
+    line = {"stage": args.stage, "config": workload_config(cfg, "n/a"), "ms": ms, "steps": args.steps,
+            "hbm_gbs": stage_bytes(cfg, args.stage) / (ms / 1000.0) / 1e9,
+            "algorithmic_bytes": stage_bytes(cfg, args.stage)}
+    if args.stage == "route":
+        line["fp32_tflops"] = 2.0 * cfg.T * cfg.d * cfg.E / (ms / 1000.0) / 1e12
+    print(json.dumps(line), flush=True)
 
 
 def main():
