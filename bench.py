@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--schedule", default="interleaved", choices=["interleaved", "wave"])
     ap.add_argument("--lead", type=int, default=0)
+    ap.add_argument("--orientation", default="default", choices=["default", "tokens-m", "tokens-n"],
+                    help="grouped GEMM operand orientation (which MMA operand holds the tokens)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--timeline", action="store_true",
@@ -320,8 +322,10 @@ def run_ours(args, cfg):
     rows = cfg.T // cfg.S
     out = [torch.empty(rows, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    orient = {"default": moe.ORIENT_DEFAULT, "tokens-m": moe.ORIENT_TOKENS_M,
+              "tokens-n": moe.ORIENT_TOKENS_N}[args.orientation]
     tuning = moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE if args.schedule == "wave"
-                        else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead)
+                        else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead, orientation=orient)
     stream = torch.cuda.current_stream(dev)
 
     def step(evs=None):
@@ -439,6 +443,8 @@ def run_ours(args, cfg):
     }
     if args.lead:
         line["config"]["lead_rows"] = args.lead
+    if args.orientation != "default":
+        line["config"]["orientation"] = args.orientation
     if args.timeline:
         line["timeline"] = timeline_summary(moe, cfg, shape, inp, ws, tuning, dev)
     print(json.dumps(line), flush=True)

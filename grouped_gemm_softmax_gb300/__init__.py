@@ -25,12 +25,13 @@ from .build import LIB_PATH
 __all__ = [
     "MoEError", "Shape", "Tuning", "library", "workspace_bytes", "workspace_region", "alloc_workspace",
     "ws_view", "route", "dispatch", "expert_ffn", "combine", "layer_forward", "last_device_status",
-    "SCHEDULE_INTERLEAVED", "SCHEDULE_EXPERT_WAVE", "WS",
+    "SCHEDULE_INTERLEAVED", "SCHEDULE_EXPERT_WAVE", "ORIENT_DEFAULT", "ORIENT_TOKENS_M", "ORIENT_TOKENS_N", "WS",
 ]
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = \
     range(6)
 SCHEDULE_INTERLEAVED, SCHEDULE_EXPERT_WAVE = 0, 1
+ORIENT_DEFAULT, ORIENT_TOKENS_M, ORIENT_TOKENS_N = 0, 1, 2
 
 
 class WS:
@@ -55,7 +56,7 @@ class _CTuning(ctypes.Structure):
                 ("l2_block_n", ctypes.c_int), ("group_rows", ctypes.c_int), ("cta_group", ctypes.c_int),
                 ("wait_limit_us", ctypes.c_int), ("unmet_dependency", ctypes.c_int),
                 ("trace", ctypes.c_void_p), ("tile_trace", ctypes.c_void_p),
-                ("tile_trace_cap", ctypes.c_int), ("reserved2", ctypes.c_int)]
+                ("tile_trace_cap", ctypes.c_int), ("orientation", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -97,13 +98,14 @@ class Tuning:
     trace: object = None  # optional torch int64 CUDA tensor of >= num_ctas * TRACE_WORDS entries
     tile_trace: object = None  # optional torch int64 CUDA tensor, num_ctas * cap * TILE_TRACE_WORDS
     tile_trace_cap: int = 0
+    orientation: int = ORIENT_DEFAULT  # which MMA operand holds the tokens (ORIENT_*)
 
     def c(self) -> _CTuning:
         tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
         tt = None if self.tile_trace is None else _ptr(self.tile_trace, torch.int64, None, "tile_trace")
         return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
                         self.cta_group, self.wait_limit_us, self.unmet_dependency, tr, tt,
-                        self.tile_trace_cap, 0)
+                        self.tile_trace_cap, self.orientation)
 
 
 _lib = None

@@ -39,6 +39,21 @@
 // TMA loads complete on the first CTA's stage barrier; both CTAs' epilogues
 // release an accumulator by arriving on the first CTA's barrier. CG = 1 keeps
 // one CTA per tile (4 stages of 48 KiB) for comparison.
+//
+// Tokens on the N side (TN, CTA pairs only). Above, tokens are the MMA's M
+// rows, so every expert's last scheduler row is padded to 256 rows. With TN the
+// operands swap: A (M, split between the pair) holds weight rows and B (N)
+// holds the scheduler row's tokens, and the MMA width N is the expert's
+// remaining tokens rounded up to 16, so an expert wastes at most 15 token
+// columns. Linear-1: each CTA's A tile is 64 W1 rows over the same 64 W3
+// rows (64 features; the pair covers 128 h columns), so tensor-memory lanes
+// 0-63 hold gate and 64-127 up: the epilogue warps reading lanes q*32.. and
+// (q+2)*32.. swap half of their 32-token slab through shared memory, the gate
+// warp then finishing tokens 0-15 and the up warp tokens 16-31. Linear-2: each
+// CTA's A tile is 128 W2 rows (256 y columns a pair). B of a tile of N tokens
+// is split as the MMA wants it: the first CTA supplies tokens [0, N/2), the
+// second [N/2, N). Each epilogue warp turns its (row, token) block around in
+// its own shared-memory slab, so that lanes store tokens' contiguous outputs.
 #include <climits>
 
 #include "kernels.cuh"
@@ -100,6 +115,7 @@ struct SmemCtl {
     uint64_t drain;              // every MMA this CTA issued has completed (teardown)
     uint32_t tmem_base;
     int abort;
+    int epi_fail;  // TN epilogue: a warp gave up (the warp pairs meet at barriers)
     int nwaves;
     int offs[kMaxExperts + 1];       // expert row offsets (copy of expert_offsets)
     int row_start[kMaxExperts + 1];  // first scheduler row of each expert
@@ -107,8 +123,9 @@ struct SmemCtl {
     int wave_tile[kMaxExperts + 1];  // first global tile index of wave w
 };
 
-// epilogue transpose buffer: per epilogue warp, 32 rows x 64 bf16 (128 B a row)
-constexpr int kEpiStageBytes = 32 * 128;
+// epilogue buffer per epilogue warp: tokens on the M side use 32 rows x 64
+// bf16 (4 KiB); tokens on the N side two 2 KiB mailboxes and a 1 KiB slab
+constexpr int kEpiStageBytes = 5 * 1024;
 constexpr size_t kCtlBytes = (sizeof(SmemCtl) + 127) / 128 * 128;
 template <int CG>
 constexpr size_t smem_bytes()
@@ -251,14 +268,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-__device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits)
+__device__ __forceinline__ float silu_mul(float g, float u)
 {
-    const float g = __uint_as_float(g_bits);
-    const float u = __uint_as_float(u_bits);
     return g * __fdividef(1.0f, 1.0f + __expf(-g)) * u;
 }
 
-template <int CG>
+__device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits)
+{
+    return silu_mul(__uint_as_float(g_bits), __uint_as_float(u_bits));
+}
+
+// MMA width (TN) of a scheduler row whose expert has `remaining` tokens from
+// the row's first token on: the row's tokens rounded up to a multiple of 16
+__device__ __forceinline__ int tile_tokens(int remaining, int rows)
+{
+    return (min(remaining, rows) + 15) & ~15;
+}
+
+template <int CG, bool TN>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_h,
@@ -281,6 +308,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int E = p.E;
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // CTA within the pair
     const bool leader = rank == 0;
+    static_assert(!TN || CG == 2, "tokens on the N side needs CTA pairs");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -294,6 +322,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
         mbar_init(&c.drain, 1);
         c.abort = 0;
+        c.epi_fail = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -392,9 +421,13 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         : nullptr;
                 unsigned long long dep0 = rec ? clock64() : 0;
                 const int e = t.e;
-                // this CTA's 128 rows of the scheduler row
-                const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows +
-                                 static_cast<int>(rank) * kBlockM;
+                const int band0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows;
+                // this CTA's 128 rows of the scheduler row (tokens on the M side)
+                const int row0 = band0 + static_cast<int>(rank) * kBlockM;
+                // this CTA's first token of B (tokens on the N side)
+                const int brow = TN ? band0 + static_cast<int>(rank) *
+                                                  (tile_tokens(c.offs[e + 1] - band0, kTileRows) >> 1)
+                                    : 0;
                 if (t.kind == 1) {
                     const unsigned long long tw = tr ? clock64() : 0;
                     if (!wait_rows_ready(&p.l1_done[t.row],
@@ -416,8 +449,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
                 // bytes of one stage summed over the CTAs of the pair
                 const uint32_t bytes =
-                    CG * (t.kind == 0 ? kATileBytes + kBTileBytes
-                                      : kATileBytes + (p.N2 / CG) * kBlockK * 2);
+                    CG * ((TN || t.kind == 0) ? kATileBytes + kBTileBytes
+                                              : kATileBytes + (p.N2 / CG) * kBlockK * 2);
                 for (int kb = 0; kb < nkb; ++kb) {
                     const unsigned long long tw = tr ? clock64() : 0;
                     if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag, p.status, kWhereProducerEmpty,
@@ -432,7 +465,19 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                  : smem_u32(&c.full[s]);
                     uint8_t *a = sA + s * kATileBytes;
                     uint8_t *b = sB + s * kBTileBytes;
-                    if (t.kind == 0) {
+                    if constexpr (TN) {
+                        if (t.kind == 0) {
+                            // 64 W1 rows over the same 64 W3 rows, then the tokens
+                            const int f = t.n * kL1N + static_cast<int>(rank) * (kL1N / 2);
+                            tma_load_3d<CG>(&tm_w1, bar, a, kb * kBlockK, f, e);
+                            tma_load_3d<CG>(&tm_w3, bar, a + kATileBytes / 2, kb * kBlockK, f, e);
+                            tma_load_2d<CG>(&tm_x, bar, b, kb * kBlockK, brow);
+                        } else {
+                            tma_load_3d<CG>(&tm_w2, bar, a, kb * kBlockK,
+                                            t.n * p.N2 + static_cast<int>(rank) * kBlockM, e);
+                            tma_load_2d<CG>(&tm_h, bar, b, kb * kBlockK, brow);
+                        }
+                    } else if (t.kind == 0) {
                         tma_load_2d<CG>(&tm_x, bar, a, kb * kBlockK, row0);
                         if (CG == 1 || rank == 0)
                             tma_load_3d<CG>(&tm_w1, bar, b, kb * kBlockK, t.n * kL1N, e);
@@ -488,7 +533,11 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 if (rec) rec[3] = clock64();
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b) * kAccCols;
-                const uint32_t idesc = t.kind == 0 ? idesc1 : idesc2;
+                uint32_t idesc = t.kind == 0 ? idesc1 : idesc2;
+                if constexpr (TN) {
+                    const int band0 = c.offs[t.e] + (t.row - c.row_start[t.e]) * kTileRows;
+                    idesc = idesc_bf16_f32(kTileRows, tile_tokens(c.offs[t.e + 1] - band0, kTileRows));
+                }
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
                 for (int kb = 0; kb < nkb; ++kb) {
                     tw = (tr || rec) ? clock64() : 0;
@@ -552,7 +601,16 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             // the whole warp agrees before its warp-collective tensor-memory loads
             const bool ready = mbar_wait(&c.tfull[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
                                          static_cast<unsigned>(tl), p.wait_ns);
-            if (!__all_sync(0xffffffffu, ready)) break;
+            bool go = __all_sync(0xffffffffu, ready);
+            if constexpr (TN) {
+                // warp pairs meet at named barriers below, so all four epilogue
+                // warps leave together or not at all (a flag only ever set, read
+                // after a barrier every warp reaches in this iteration)
+                if (!go && lane == 0) c.epi_fail = 1;
+                named_bar_sync(1, kEpiThreads);
+                go = *reinterpret_cast<volatile int *>(&c.epi_fail) == 0;
+            }
+            if (!go) break;
             unsigned long long *rec =
                 (publisher && p.tile_trace && tl < p.tile_trace_cap)
                     ? p.tile_trace + (static_cast<long>(blockIdx.x) * p.tile_trace_cap + tl) * kTileTraceWords
@@ -569,52 +627,142 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int e = t.e;
             const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows +
                              static_cast<int>(rank) * kBlockM;
-            const int valid_rows = min(kBlockM, c.offs[e + 1] - row0);  // may be <= 0
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(b) * kAccCols;
-            // 64 columns at a time: tensor memory -> registers (thread = row) ->
-            // swizzled shared-memory transpose -> 16-byte stores that cover four
-            // full 128-byte row segments per warp instruction.
-            uint8_t *stg = s_epi + (warp - 2) * kEpiStageBytes;
-            const int nchunks = t.kind == 0 ? kL1N / 64 : p.N2 / 64;
-            uint16_t *const out_base = t.kind == 0 ? p.h : p.y;
-            const int out_ld = t.kind == 0 ? p.F : p.d;
-            const int col_base = t.kind == 0 ? t.n * kL1N : t.n * p.N2;
-            for (int ch = 0; ch < nchunks; ++ch) {
-                uint32_t pk[32];
-                if (t.kind == 0) {
-                    uint32_t g[64], u[64];
-                    tmem_load_2x64cols(tbase + ch * 64, tbase + kL1N + ch * 64, g, u);
+            if constexpr (TN) {
+                // accumulator: lane = weight row, column = token. Per 32-token
+                // slab each warp works alone: Linear-1 lanes l and l+16 hold
+                // gate and up of one feature, one shuffle gives lane l tokens
+                // 0-15 and lane l+16 tokens 16-31 of that feature; the bf16
+                // results go token-major into the warp's shared-memory slab,
+                // and lane j stores token j's contiguous columns.
+                const int band0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows;
+                const int valid = min(kTileRows, c.offs[e + 1] - band0);
+                uint8_t *wslab = s_epi + (warp - 2) * kEpiStageBytes;
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                    static_cast<uint32_t>(b) * kAccCols;
+                const int nch = (valid + 31) >> 5;
+                for (int ch = 0; ch < nch; ++ch) {
+                    uint32_t v[32];
+                    tmem_load_32cols(tb + ch * 32, v);
+                    const long grow = static_cast<long>(band0) + ch * 32 + lane;  // token row of this lane
+                    const bool store = ch * 32 + lane < valid;
+                    if (t.kind == 0) {
+                        // q < 2: gate of features 32q + lane, finishes tokens 0-15;
+                        // q >= 2: up of features 32(q-2) + lane, finishes tokens 16-31.
+                        // Each warp sends the other half through its double-buffered
+                        // 2 KiB mailbox ([16 tokens][32 lanes] fp32), then one
+                        // barrier of the warp pair.
+                        const bool gate_w = q < 2;
+                        float *mine = reinterpret_cast<float *>(wslab + (ch & 1) * 2048);
+                        const int pw = (q ^ 2) < 2 ? (q ^ 2) + 4 : (q ^ 2);  // partner warp (quarter q ^ 2)
+                        const float *theirs = reinterpret_cast<const float *>(
+                            s_epi + (pw - 2) * kEpiStageBytes + (ch & 1) * 2048);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        pk[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]),
-                                            silu_mul(g[2 * i + 1], u[2 * i + 1]));
-                } else {
-                    uint32_t a[64];
-                    tmem_load_64cols(tbase + ch * 64, a);
+                        for (int i = 0; i < 16; ++i)
+                            mine[i * 32 + lane] = __uint_as_float(gate_w ? v[16 + i] : v[i]);
+                        named_bar_sync(2 + (q & 1), 64);
+                        float hv[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                        for (int i = 0; i < 16; ++i) {
+                            const float other = theirs[i * 32 + lane];
+                            hv[i] = gate_w ? silu_mul(__uint_as_float(v[i]), other)
+                                           : silu_mul(other, __uint_as_float(v[16 + i]));
+                        }
+                        // bf16 pairs of adjacent features, token-major: even lane
+                        // takes token 2i, odd lane token 2i+1 ([16 tokens][16 words])
+                        uint32_t *sl = reinterpret_cast<uint32_t *>(wslab + 4096);
+                        const bool ev = (lane & 1) == 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float r = __shfl_xor_sync(0xffffffffu, ev ? hv[2 * i + 1] : hv[2 * i], 1);
+                            sl[(2 * i + (ev ? 0 : 1)) * 16 + (lane >> 1)] =
+                                ev ? pack_bf16x2(hv[2 * i], r) : pack_bf16x2(r, hv[2 * i + 1]);
+                        }
+                        __syncwarp();
+                        // two lanes a token, 32 bytes each
+                        const int tk = (gate_w ? 0 : 16) + (lane >> 1);
+                        const int half = lane & 1;
+                        const int col = t.n * kL1N + static_cast<int>(rank) * (kL1N / 2) + (q & 1) * 32 +
+                                        half * 16;
+                        const long hrow = static_cast<long>(band0) + ch * 32 + tk;
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int j = jj ^ ((lane >> 2) & 1);  // spread the lanes over the banks
+                            const uint4 val = *reinterpret_cast<const uint4 *>(
+                                reinterpret_cast<const uint8_t *>(sl) + (tk & 15) * 64 + half * 32 + j * 16);
+                            if (ch * 32 + tk < valid && col + 8 * j < p.F)
+                                *reinterpret_cast<uint4 *>(p.h + hrow * p.F + col + 8 * j) = val;
+                        }
+                    } else {
+                        // even lane: (row, row+1) of token 2i; odd lane: of token 2i+1
+                        const bool ev = (lane & 1) == 0;
+                        uint32_t *sl = reinterpret_cast<uint32_t *>(wslab);  // [32 tokens][16 words]
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const uint32_t r = __shfl_xor_sync(0xffffffffu, ev ? v[2 * i + 1] : v[2 * i], 1);
+                            const float lo_v = __uint_as_float(ev ? v[2 * i] : r);
+                            const float hi_v = __uint_as_float(ev ? r : v[2 * i + 1]);
+                            sl[(2 * i + (ev ? 0 : 1)) * 16 + (lane >> 1)] = pack_bf16x2(lo_v, hi_v);
+                        }
+                        __syncwarp();
+                        const int col = t.n * p.N2 + static_cast<int>(rank) * kBlockM + q * 32;
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = (jj + (lane >> 1)) & 3;  // spread the lanes over the banks
+                            const uint4 val = *reinterpret_cast<const uint4 *>(wslab + lane * 64 + j * 16);
+                            if (store && col + 8 * j < p.d)
+                                *reinterpret_cast<uint4 *>(p.y + grow * p.d + col + 8 * j) = val;
+                        }
+                    }
+                    __syncwarp();
                 }
-                // row `lane` of the warp's 32-row slab: 8 pieces of 16 B, piece j at
-                // slot j ^ (lane & 7) (conflict-free writes and reads)
+            } else {
+                const int valid_rows = min(kBlockM, c.offs[e + 1] - row0);  // may be <= 0
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(b) * kAccCols;
+                // 64 columns at a time: tensor memory -> registers (thread = row) ->
+                // swizzled shared-memory transpose -> 16-byte stores that cover four
+                // full 128-byte row segments per warp instruction.
+                uint8_t *stg = s_epi + (warp - 2) * kEpiStageBytes;
+                const int nchunks = t.kind == 0 ? kL1N / 64 : p.N2 / 64;
+                uint16_t *const out_base = t.kind == 0 ? p.h : p.y;
+                const int out_ld = t.kind == 0 ? p.F : p.d;
+                const int col_base = t.kind == 0 ? t.n * kL1N : t.n * p.N2;
+                for (int ch = 0; ch < nchunks; ++ch) {
+                    uint32_t pk[32];
+                    if (t.kind == 0) {
+                        uint32_t g[64], u[64];
+                        tmem_load_2x64cols(tbase + ch * 64, tbase + kL1N + ch * 64, g, u);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                __syncwarp();
-                const int piece = lane & 7;
-                const int col = col_base + ch * 64 + piece * 8;
+                        for (int i = 0; i < 32; ++i)
+                            pk[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]),
+                                                silu_mul(g[2 * i + 1], u[2 * i + 1]));
+                    } else {
+                        uint32_t a[64];
+                        tmem_load_64cols(tbase + ch * 64, a);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = i * 4 + (lane >> 3);  // row within the warp's slab
-                    const uint4 v =
-                        *reinterpret_cast<const uint4 *>(stg + r * 128 + ((piece ^ (r & 7)) << 4));
-                    if (q * 32 + r < valid_rows && col < out_ld)
-                        *reinterpret_cast<uint4 *>(out_base + (static_cast<long>(row0) + q * 32 + r) *
-                                                                  out_ld + col) = v;
+                        for (int i = 0; i < 32; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                    }
+                    // row `lane` of the warp's 32-row slab: 8 pieces of 16 B, piece j at
+                    // slot j ^ (lane & 7) (conflict-free writes and reads)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    __syncwarp();
+                    const int piece = lane & 7;
+                    const int col = col_base + ch * 64 + piece * 8;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = i * 4 + (lane >> 3);  // row within the warp's slab
+                        const uint4 v =
+                            *reinterpret_cast<const uint4 *>(stg + r * 128 + ((piece ^ (r & 7)) << 4));
+                        if (q * 32 + r < valid_rows && col < out_ld)
+                            *reinterpret_cast<uint4 *>(out_base + (static_cast<long>(row0) + q * 32 + r) *
+                                                                      out_ld + col) = v;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             // this thread's stores before any later TMA read of them (other CTAs)
             fence_proxy_async_global();
@@ -730,7 +878,7 @@ long ffn_max_rows(long R, int E)
 
 namespace {
 
-template <int CG>
+template <int CG, bool TN>
 cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
 {
     constexpr size_t smem = smem_bytes<CG>();
@@ -750,7 +898,7 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel<CG>,
+        cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel<CG, TN>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
         if (err != cudaSuccess) return err;
@@ -758,7 +906,7 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
         // Linear-2 tiles wait on Linear-1 tiles of other CTAs)
         int clusters = 0;
         cfg.gridDim = dim3(static_cast<unsigned>(sms / CG * CG), 1, 1);
-        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG>, &cfg);
+        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG, TN>, &cfg);
         if (err != cudaSuccess) return err;
         max_instances = clusters < sms / CG ? clusters : sms / CG;
         if (max_instances <= 0) return cudaErrorInvalidConfiguration;
@@ -769,20 +917,22 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
         const int want = a.num_ctas / CG > 0 ? a.num_ctas / CG : 1;
         if (want < instances) instances = want;
     }
-    // minimum lead of Linear-1 over Linear-2 (scheduler rows): a raster group
-    // (every tile of a row sits below position (row + group) * P1) plus the
-    // rows the instances have in flight, plus one row of margin. Never below
-    // the group size: that bound keeps the dependency waits deadlock-free.
-    p.lead = a.lead > 0 ? a.lead : p.group + (instances + p.P1 - 1) / p.P1 + 1;
+    // lead of Linear-1 over Linear-2 (scheduler rows). The minimum is a raster
+    // group (every tile of a row sits below position (row + group) * P1) plus
+    // the rows the instances have in flight; tiles finish out of order, and
+    // below about twice that Linear-2 producers start to wait, so the default
+    // is twice the minimum plus one row. Never below the group size: that
+    // bound keeps the dependency waits deadlock-free.
+    p.lead = a.lead > 0 ? a.lead : 2 * (p.group + (instances + p.P1 - 1) / p.P1) + 1;
     if (p.lead < p.group) p.lead = p.group;
 
     const long R = a.R;
     CUtensorMap tx, th, tw1, tw3, tw2;
     if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, kBlockM) ||
         !make_map_2d(&th, a.h, a.F, R, kBlockK, kBlockM) ||
-        !make_map_3d(&tw1, a.w1, a.d, a.F, a.E, kBlockK, kL1N) ||
-        !make_map_3d(&tw3, a.w3, a.d, a.F, a.E, kBlockK, kL1N) ||
-        !make_map_3d(&tw2, a.w2, a.F, a.d, a.E, kBlockK, p.N2 / CG))
+        !make_map_3d(&tw1, a.w1, a.d, a.F, a.E, kBlockK, TN ? kL1N / 2 : kL1N) ||
+        !make_map_3d(&tw3, a.w3, a.d, a.F, a.E, kBlockK, TN ? kL1N / 2 : kL1N) ||
+        !make_map_3d(&tw2, a.w2, a.F, a.d, a.E, kBlockK, TN ? kBlockM : p.N2 / CG))
         return cudaErrorInvalidValue;
 
     if (!a.counters_zeroed) {
@@ -790,7 +940,7 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
         if (err != cudaSuccess) return err;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(instances * CG), 1, 1);
-    return cudaLaunchKernelEx(&cfg, grouped_swiglu_gemm_kernel<CG>, tx, th, tw1, tw3, tw2, p);
+    return cudaLaunchKernelEx(&cfg, grouped_swiglu_gemm_kernel<CG, TN>, tx, th, tw1, tw3, tw2, p);
 }
 
 }  // namespace
@@ -809,7 +959,26 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.d = a.d;
     p.F = a.F;
     p.R = a.R;
-    p.N2 = ffn_l2_block_n(a.d, a.l2_block_n);
+    // CTA pairs halve the operand traffic per MMA. With tokens on the M side
+    // they pad every expert to 256-row tiles, so below ~1024 rows per expert
+    // single CTAs win there; with tokens on the N side (pairs only) an expert
+    // pads to 16 tokens. Tokens go on the N side unless Linear-2's 256-wide
+    // weight tiles would pad y (d not a multiple of 256) on large experts.
+    const bool big_experts = a.R / a.E >= 1024;
+    bool tn;
+    if (a.orientation == 2)
+        tn = true;
+    else if (a.orientation == 1 || a.cta_group == 1)
+        tn = false;
+    else
+        tn = a.d % 256 == 0 || !big_experts;
+    if (tn)
+        p.cg = 2;
+    else if (a.cta_group == 1 || a.cta_group == 2)
+        p.cg = a.cta_group;
+    else
+        p.cg = big_experts ? 2 : 1;
+    p.N2 = tn ? 2 * kBlockM : ffn_l2_block_n(a.d, a.l2_block_n);
     p.P1 = (a.F + kL1N - 1) / kL1N;
     p.P2 = (a.d + p.N2 - 1) / p.N2;
     p.kb1 = (a.d + kBlockK - 1) / kBlockK;
@@ -822,16 +991,11 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.wait_ns = a.wait_limit_us > 0 ? 1000ull * static_cast<unsigned long long>(a.wait_limit_us)
                                     : kWaitLimitNs;
     p.unmet_dependency = a.unmet_dependency > 0 ? 1 : 0;
-    // CTA pairs halve the operand traffic per MMA but pad every expert to
-    // 256-row tiles; below ~1024 rows per expert the padding costs more
-    if (a.cta_group == 1 || a.cta_group == 2)
-        p.cg = a.cta_group;
-    else
-        p.cg = a.R / a.E >= 1024 ? 2 : 1;
     const int group = a.group_rows > 0 ? a.group_rows : kDefaultGroupRows;  // 128-row M-tiles
     p.group = (group + p.cg - 1) / p.cg;                                     // scheduler rows
-    if (p.cg == 1) return launch_cg<1>(a, p, stream);
-    return launch_cg<2>(a, p, stream);
+    if (tn) return launch_cg<2, true>(a, p, stream);
+    if (p.cg == 1) return launch_cg<1, false>(a, p, stream);
+    return launch_cg<2, false>(a, p, stream);
 }
 
 }  // namespace moe

@@ -54,6 +54,7 @@ struct FfnArgs {
     long max_rows;
     int R, d, F, E;
     int schedule, lead, num_ctas, l2_block_n, group_rows, cta_group;
+    int orientation;  // 0 = choose, 1 = tokens on the MMA's M side, 2 = on its N side
     int wait_limit_us, unmet_dependency;
     unsigned long long *trace;  // optional per-CTA counters (16 per CTA)
     unsigned long long *tile_trace;  // optional per-tile timeline (8 words per tile)

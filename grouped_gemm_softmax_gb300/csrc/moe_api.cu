@@ -136,7 +136,8 @@ moe_status_t check_tuning(const moe_tuning_t *t)
         return MOE_ERR_INVALID_ARG;
     if (t->tile_trace && (t->tile_trace_cap <= 0 || (reinterpret_cast<uintptr_t>(t->tile_trace) & 7u)))
         return MOE_ERR_INVALID_ARG;
-    if (t->reserved2 != 0) return MOE_ERR_INVALID_ARG;
+    if (t->orientation < 0 || t->orientation > 2) return MOE_ERR_INVALID_ARG;
+    if (t->orientation == 2 && t->cta_group == 1) return MOE_ERR_INVALID_ARG;
     if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
@@ -168,6 +169,7 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.l2_block_n = tune ? tune->l2_block_n : 0;
     a.group_rows = tune ? tune->group_rows : 0;
     a.cta_group = tune ? tune->cta_group : 0;
+    a.orientation = tune ? tune->orientation : 0;
     a.wait_limit_us = tune ? tune->wait_limit_us : 0;
     a.unmet_dependency = tune ? tune->unmet_dependency : 0;
     a.trace = tune ? static_cast<unsigned long long *>(tune->trace) : nullptr;

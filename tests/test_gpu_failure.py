@@ -33,8 +33,12 @@ def _case(counts, d, F):
     return counts, off, x, w1, w3, w2
 
 
-@pytest.mark.parametrize("cg", [1, 2])
-def test_unmet_dependency_times_out_and_the_context_survives(cg):
+MODES = [dict(cta_group=1, orientation=moe.ORIENT_TOKENS_M), dict(cta_group=2, orientation=moe.ORIENT_TOKENS_M),
+         dict(cta_group=2, orientation=moe.ORIENT_TOKENS_N)]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=["m1", "m2", "n2"])
+def test_unmet_dependency_times_out_and_the_context_survives(mode):
     need_gpu()
     counts, off, x, w1, w3, w2 = _case([300, 40, 0, 513], 256, 384)
     E, R, d, F = len(counts), int(counts.sum()), 256, 384
@@ -43,7 +47,7 @@ def test_unmet_dependency_times_out_and_the_context_survives(cg):
     y = torch.zeros(R, d, dtype=torch.bfloat16, device="cuda")
     t0 = time.time()
     moe.expert_ffn(s, x, off, w1, w3, w2, y, ws,
-                   tuning=moe.Tuning(cta_group=cg, wait_limit_us=20000, unmet_dependency=1))
+                   tuning=moe.Tuning(**mode, wait_limit_us=20000, unmet_dependency=1))
     st = moe.last_device_status(ws)
     elapsed = time.time() - t0
     assert st == moe.MOE_ERR_TIMEOUT
@@ -53,7 +57,7 @@ def test_unmet_dependency_times_out_and_the_context_survives(cg):
     assert moe.last_device_status(ws) == moe.MOE_OK  # reading it cleared it
 
     # the same context runs the normal call correctly afterwards
-    moe.expert_ffn(s, x, off, w1, w3, w2, y, ws, tuning=moe.Tuning(cta_group=cg))
+    moe.expert_ffn(s, x, off, w1, w3, w2, y, ws, tuning=moe.Tuning(**mode))
     assert moe.last_device_status(ws) == moe.MOE_OK
     er = np.repeat(np.arange(E), counts).astype(np.int32)
     _, yref = oracle.ffn_rows(bits(x), er, bits(w1), bits(w3), bits(w2), E)

@@ -1,7 +1,9 @@
 """GPU grouped SwiGLU GEMM (moe_expert_ffn) against the oracle's per-row expert
 FFN: h and y_perm within the bf16 tolerances, on ragged expert sizes (empty
-experts, one-row experts, tiles that straddle experts, K and N tails), both
-tile schedules bit-identical, and every Linear-2 tile's ready flag published."""
+experts, one-row experts, tiles that straddle experts, K and N tails) in both
+operand orientations (tokens as the MMA's M rows or as its N columns), every
+tile schedule bit-identical within an orientation, and every Linear-2 tile's
+ready flag published."""
 import numpy as np
 import pytest
 import torch
@@ -58,30 +60,39 @@ CASES = {
 }
 
 
+# (CTAs per tile, operand orientation): single CTAs and pairs with tokens as M
+# rows, pairs with tokens as N columns
+MODES = {"m1": dict(cta_group=1, orientation=moe.ORIENT_TOKENS_M),
+         "m2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_M),
+         "n2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_N)}
+TILE_ROWS = {"m1": 128, "m2": 256, "n2": 256}
+
+
+@pytest.mark.parametrize("mode", ["m1", "n2"])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_ffn_parity(name):
+def test_ffn_parity(name, mode):
     need_gpu()
     counts, d, F = CASES[name]
     c = make_case(counts, d, F, seed=len(name))
-    _, _, h, y = run_ffn(c)
+    _, _, h, y = run_ffn(c, tuning=moe.Tuning(**MODES[mode]))
     rows = np.arange(c["R"])
     href, yref = oracle_rows(c, rows)
-    assert_close(to_f64(h), href, f"{name} h")
-    assert_close(to_f64(y), yref, f"{name} y")
+    assert_close(to_f64(h), href, f"{name} {mode} h")
+    assert_close(to_f64(y), yref, f"{name} {mode} y")
 
 
-@pytest.mark.parametrize("cg", [1, 2])
-def test_ffn_schedules_and_grids_are_bit_identical(cg):
+@pytest.mark.parametrize("mode", sorted(MODES))
+def test_ffn_schedules_and_grids_are_bit_identical(mode):
     """The tile order never changes a result: every schedule, lead, raster group
-    and grid size gives the same bits (within one CTA-group size)."""
+    and grid size gives the same bits (within one tile shape)."""
     need_gpu()
     c = make_case([70, 0, 129, 1, 255, 57, 300, 12] * 4, 256, 384, seed=9)
-    _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(cta_group=cg))
+    _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(**MODES[mode]))
     variants = [dict(schedule=moe.SCHEDULE_EXPERT_WAVE), dict(lead_rows=1), dict(lead_rows=50),
                 dict(num_ctas=2), dict(num_ctas=7), dict(group_rows=1), dict(group_rows=4),
                 dict(schedule=moe.SCHEDULE_EXPERT_WAVE, num_ctas=6, group_rows=2)]
     for v in variants:
-        t = moe.Tuning(cta_group=cg, **v)
+        t = moe.Tuning(**MODES[mode], **v)
         _, _, h, y = run_ffn(c, tuning=t)
         assert torch.equal(h.view(torch.int16), h0.view(torch.int16)), t
         assert torch.equal(y.view(torch.int16), y0.view(torch.int16)), t
@@ -90,8 +101,8 @@ def test_ffn_schedules_and_grids_are_bit_identical(cg):
 def test_cta_pairs_match_single_ctas():
     need_gpu()
     c = make_case([70, 0, 129, 1, 255, 57, 300, 12], 256, 384, seed=10)
-    _, _, h1, y1 = run_ffn(c, tuning=moe.Tuning(cta_group=1))
-    _, _, h2, y2 = run_ffn(c, tuning=moe.Tuning(cta_group=2))
+    _, _, h1, y1 = run_ffn(c, tuning=moe.Tuning(**MODES["m1"]))
+    _, _, h2, y2 = run_ffn(c, tuning=moe.Tuning(**MODES["m2"]))
     href, yref = oracle_rows(c, np.arange(c["R"]))
     assert_close(to_f64(h2), href, "pairs h")
     assert_close(to_f64(y2), yref, "pairs y")
@@ -100,23 +111,51 @@ def test_cta_pairs_match_single_ctas():
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
 
 
+def test_tokens_as_n_columns_match_tokens_as_m_rows():
+    """Swapping the MMA operands changes only the fp32 accumulation order: both
+    orientations meet the oracle, and agree with each other to a few bf16 ulps."""
+    need_gpu()
+    c = make_case([70, 0, 129, 1, 255, 57, 300, 12, 16, 17, 15], 512, 640, seed=11)
+    _, _, hm, ym = run_ffn(c, tuning=moe.Tuning(**MODES["m2"]))
+    _, _, hn, yn = run_ffn(c, tuning=moe.Tuning(**MODES["n2"]))
+    href, yref = oracle_rows(c, np.arange(c["R"]))
+    assert_close(to_f64(hn), href, "tokens-as-N h")
+    assert_close(to_f64(yn), yref, "tokens-as-N y")
+    # each result is the bf16 rounding of nearly the same fp32 value
+    for a, b in ((hm, hn), (ym, yn)):
+        da, db = to_f64(a), to_f64(b)
+        assert np.all(np.abs(da - db) <= 2.0 ** -6 * np.abs(da) + 1e-6)
+
+
+def test_default_orientation_puts_tokens_on_n_for_small_experts():
+    """The default for 300-row experts is tokens as N columns: bit-identical to
+    asking for it."""
+    need_gpu()
+    c = make_case([300, 200, 280], 256, 256, seed=12)
+    _, _, hd, yd = run_ffn(c)
+    _, _, hn, yn = run_ffn(c, tuning=moe.Tuning(orientation=moe.ORIENT_TOKENS_N))
+    assert torch.equal(yd.view(torch.int16), yn.view(torch.int16))
+
+
 @pytest.mark.parametrize("n2", [64, 128, 192, 256])
 def test_ffn_l2_tile_widths(n2):
     need_gpu()
     c = make_case([150, 90], 384, 256, seed=n2)
-    _, _, h, y = run_ffn(c, tuning=moe.Tuning(l2_block_n=n2))
+    _, _, h, y = run_ffn(c, tuning=moe.Tuning(l2_block_n=n2, orientation=moe.ORIENT_TOKENS_M))
     href, yref = oracle_rows(c, np.arange(c["R"]))
     assert_close(to_f64(y), yref, f"N2={n2} y")
 
 
-@pytest.mark.parametrize("cg", [1, 2])
-def test_ready_flags_carry_the_call_epoch(cg):
+@pytest.mark.parametrize("mode", sorted(MODES))
+def test_ready_flags_carry_the_call_epoch(mode):
     need_gpu()
     counts = [70, 0, 129, 1, 255]
     c = make_case(counts, 256, 256, seed=4)
-    t = moe.Tuning(cta_group=cg)
+    t = moe.Tuning(**MODES[mode])
+    cg = MODES[mode]["cta_group"]
     s, ws, _, _ = run_ffn(c, tuning=t)
-    rows = int(sum((n + 128 * cg - 1) // (128 * cg) for n in counts))  # scheduler rows
+    tr = TILE_ROWS[mode]
+    rows = int(sum((n + tr - 1) // tr for n in counts))  # scheduler rows
     p2 = 1  # d = 256 -> one 256-wide Linear-2 tile per row
     nflags = rows * p2 * cg  # one flag per CTA of each Linear-2 tile
     flags = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (nflags,)).cpu().numpy()
