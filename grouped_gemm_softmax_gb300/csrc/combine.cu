@@ -10,7 +10,7 @@
 // combine would send as one contiguous block per rank.
 //
 // One warp per token; each lane owns 16-byte column vectors (8 bf16), loads the
-// k expert rows with 128-bit loads and accumulates in fp32.
+// k expert rows with 128-bit loads and accumulates in fp32 in j order.
 #include "kernels.cuh"
 
 namespace moe {
@@ -38,39 +38,50 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// KMAX bounds k; each lane keeps U = 8 / KMAX column vectors of every expert
+// row in flight (16 loads of 16 bytes at most), so a small k still has enough
+// memory-level parallelism to cover HBM latency.
+template <int KMAX>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ gate,
                const int32_t *__restrict__ row_of_slot, int T, int d, int k, int rows_per_seg,
                const Segments seg)
 {
+    constexpr int U = 8 / KMAX;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long t = static_cast<long>(blockIdx.x) * (kThreads / 32) + warp;
     if (t >= T) return;
-    int rows[kMaxTopK];
-    float g[kMaxTopK];
+    const uint4 *src[KMAX];
+    float g[KMAX];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        rows[j] = j < k ? row_of_slot[t * k + j] : -1;
+    for (int j = 0; j < KMAX; ++j) {
+        src[j] = j < k ? reinterpret_cast<const uint4 *>(y + static_cast<long>(row_of_slot[t * k + j]) * d)
+                       : nullptr;
         g[j] = j < k ? gate[t * k + j] : 0.0f;
     }
-    uint16_t *dst = seg.p[t / rows_per_seg] + (t % rows_per_seg) * static_cast<long>(d);
+    uint4 *dst = reinterpret_cast<uint4 *>(seg.p[t / rows_per_seg] + (t % rows_per_seg) * static_cast<long>(d));
     const int nvec = d / 8;
-    for (int v = lane; v < nvec; v += 32) {
-        uint4 val[kMaxTopK];
+    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+        uint4 val[U][KMAX];
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (rows[j] >= 0)
-                val[j] = reinterpret_cast<const uint4 *>(y + static_cast<long>(rows[j]) * d)[v];
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (rows[j] >= 0) acc_bf16x8(acc, val[j], g[j]);
-        uint4 o;
-        o.x = pack2(acc[0], acc[1]);
-        o.y = pack2(acc[2], acc[3]);
-        o.z = pack2(acc[4], acc[5]);
-        o.w = pack2(acc[6], acc[7]);
-        reinterpret_cast<uint4 *>(dst)[v] = o;
+            for (int j = 0; j < KMAX; ++j)
+                if (j < k && v0 + 32 * u < nvec) val[u][j] = src[j][v0 + 32 * u];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (v0 + 32 * u >= nvec) break;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (j < k) acc_bf16x8(acc, val[u][j], g[j]);
+            uint4 o;
+            o.x = pack2(acc[0], acc[1]);
+            o.y = pack2(acc[2], acc[3]);
+            o.z = pack2(acc[4], acc[5]);
+            o.w = pack2(acc[6], acc[7]);
+            dst[v0 + 32 * u] = o;
+        }
     }
 }
 
@@ -82,8 +93,12 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s)
     Segments seg;
     for (int i = 0; i < kMaxSegments; ++i) seg.p[i] = i < a.S ? a.seg[i] : nullptr;
     const unsigned blocks = static_cast<unsigned>((a.T + kThreads / 32 - 1) / (kThreads / 32));
-    combine_kernel<<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S,
-                                              seg);
+    if (a.k <= 2)
+        combine_kernel<2><<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S, seg);
+    else if (a.k <= 4)
+        combine_kernel<4><<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S, seg);
+    else
+        combine_kernel<8><<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S, seg);
     return cudaGetLastError();
 }
 
