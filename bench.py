@@ -56,6 +56,8 @@ def parse_args():
                     help="grouped GEMM operand orientation (which MMA operand holds the tokens)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--h-ring", type=int, default=0,
+                    help="h as a ring of this many scheduler rows (0 = every row in place)")
     ap.add_argument("--timeline", action="store_true",
                     help="after the timed region, run one traced grouped GEMM and add its "
                          "per-tile timeline summary to the line")
@@ -318,14 +320,15 @@ def run_ours(args, cfg):
     inp = synth.make_inputs(cfg, seed=0, device=dev)
     if rank > 0:  # each replica routes its own tokens
         inp.x = synth.gaussian_bf16((cfg.T, cfg.d), 1.0, rank, synth.TID_X, dev)
-    ws = moe.alloc_workspace(shape, dev)
-    rows = cfg.T // cfg.S
-    out = [torch.empty(rows, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     orient = {"default": moe.ORIENT_DEFAULT, "tokens-m": moe.ORIENT_TOKENS_M,
               "tokens-n": moe.ORIENT_TOKENS_N}[args.orientation]
     tuning = moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE if args.schedule == "wave"
-                        else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead, orientation=orient)
+                        else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead, orientation=orient,
+                        h_ring_rows=args.h_ring)
+    ws = moe.alloc_workspace(shape, dev, tuning if args.h_ring else None)
+    rows = cfg.T // cfg.S
+    out = [torch.empty(rows, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(evs=None):
@@ -445,6 +448,9 @@ def run_ours(args, cfg):
         line["config"]["lead_rows"] = args.lead
     if args.orientation != "default":
         line["config"]["orientation"] = args.orientation
+    if args.h_ring:
+        line["config"]["h_ring_rows"] = args.h_ring
+        line["workspace_bytes"] = int(ws.numel())
     if args.timeline:
         line["timeline"] = timeline_summary(moe, cfg, shape, inp, ws, tuning, dev)
     print(json.dumps(line), flush=True)

@@ -56,7 +56,8 @@ class _CTuning(ctypes.Structure):
                 ("l2_block_n", ctypes.c_int), ("group_rows", ctypes.c_int), ("cta_group", ctypes.c_int),
                 ("wait_limit_us", ctypes.c_int), ("unmet_dependency", ctypes.c_int),
                 ("trace", ctypes.c_void_p), ("tile_trace", ctypes.c_void_p),
-                ("tile_trace_cap", ctypes.c_int), ("orientation", ctypes.c_int)]
+                ("tile_trace_cap", ctypes.c_int), ("orientation", ctypes.c_int),
+                ("h_ring_rows", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -99,13 +100,14 @@ class Tuning:
     tile_trace: object = None  # optional torch int64 CUDA tensor, num_ctas * cap * TILE_TRACE_WORDS
     tile_trace_cap: int = 0
     orientation: int = ORIENT_DEFAULT  # which MMA operand holds the tokens (ORIENT_*)
+    h_ring_rows: int = 0  # h as a ring of this many scheduler rows (0 = all rows)
 
     def c(self) -> _CTuning:
         tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
         tt = None if self.tile_trace is None else _ptr(self.tile_trace, torch.int64, None, "tile_trace")
         return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
                         self.cta_group, self.wait_limit_us, self.unmet_dependency, tr, tt,
-                        self.tile_trace_cap, self.orientation)
+                        self.tile_trace_cap, self.orientation, self.h_ring_rows)
 
 
 _lib = None
@@ -126,6 +128,9 @@ def library():
             "moe_workspace_bytes": ([S], sz),
             "moe_workspace_region": ([S, ctypes.c_int, ctypes.POINTER(sz), ctypes.POINTER(sz)],
                                      ctypes.c_int),
+            "moe_workspace_bytes_tuned": ([S, TU], sz),
+            "moe_workspace_region_tuned": ([S, TU, ctypes.c_int, ctypes.POINTER(sz), ctypes.POINTER(sz)],
+                                           ctypes.c_int),
             "moe_route": ([S, P, P, P, P, P, P], ctypes.c_int),
             "moe_dispatch": ([S, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "moe_expert_ffn": ([S, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
@@ -183,19 +188,27 @@ def _ptr(t, dtype, numel=None, name="tensor", optional=False):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def workspace_bytes(shape: Shape) -> int:
-    return int(library().moe_workspace_bytes(ctypes.byref(shape.c())))
+def workspace_bytes(shape: Shape, tuning: Tuning | None = None) -> int:
+    if tuning is None:
+        return int(library().moe_workspace_bytes(ctypes.byref(shape.c())))
+    return int(library().moe_workspace_bytes_tuned(ctypes.byref(shape.c()), ctypes.byref(tuning.c())))
 
 
-def workspace_region(shape: Shape, region: int):
+def workspace_region(shape: Shape, region: int, tuning: Tuning | None = None):
     off, nb = ctypes.c_size_t(), ctypes.c_size_t()
-    _check(library().moe_workspace_region(ctypes.byref(shape.c()), region, ctypes.byref(off),
-                                          ctypes.byref(nb)), "moe_workspace_region")
+    if tuning is None:
+        _check(library().moe_workspace_region(ctypes.byref(shape.c()), region, ctypes.byref(off),
+                                              ctypes.byref(nb)), "moe_workspace_region")
+    else:
+        _check(library().moe_workspace_region_tuned(ctypes.byref(shape.c()), ctypes.byref(tuning.c()),
+                                                    region, ctypes.byref(off), ctypes.byref(nb)),
+               "moe_workspace_region_tuned")
     return off.value, nb.value
 
 
-def alloc_workspace(shape: Shape, device="cuda") -> torch.Tensor:
-    nb = workspace_bytes(shape)
+def alloc_workspace(shape: Shape, device="cuda", tuning: Tuning | None = None) -> torch.Tensor:
+    """Device workspace for one shape (and tuning: an h ring shrinks it)."""
+    nb = workspace_bytes(shape, tuning)
     if nb == 0:
         raise MoEError(MOE_ERR_INVALID_ARG, "moe_workspace_bytes")
     ws = torch.empty(nb, dtype=torch.uint8, device=device)

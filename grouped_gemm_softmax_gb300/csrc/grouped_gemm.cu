@@ -16,6 +16,15 @@
 // producer of a Linear-2 tile waits (acquire, bounded) until it reaches P1.
 // Each finished Linear-2 tile publishes its ready flag (= the call's epoch).
 //
+// h ring (optional, Xian et al., Algorithm 1's "destination ring slot"): h
+// holds Q scheduler rows instead of all of them; row p lives in slot p mod Q.
+// A Linear-1 tile of row p >= Q first waits (acquire, bounded) until every
+// Linear-2 tile of row p - Q has finished (l2_done[p - Q] = CTAs per tile *
+// P2), so the slot's previous rows have been read. With Q >= D + group + 1
+// every such Linear-2 tile sits before the waiting tile in every instance's
+// sequence (an instance emits all its Linear-2 tiles of row r before any
+// Linear-1 tile past row r + D), so these waits cannot deadlock either.
+//
 // Order (Xian et al., Algorithm 1, read for unpaired CTAs): CTA g of G walks two
 // cursors k1, k2 (start g, step G) over the Linear-1 and Linear-2 tile streams
 // (row-major over (row, n)); it emits the Linear-2 tile at k2 when its row
@@ -92,12 +101,14 @@ struct GemmParams {
     uint16_t *h;
     uint16_t *y;
     unsigned *l1_done;
+    unsigned *l2_done;  // per scheduler row: finished Linear-2 tiles (h ring only)
     unsigned *l2_flags;
     unsigned *status;
     int E, d, F, R;
     int P1, P2, N2;
     int kb1, kb2;
     int schedule, lead, group, cg;
+    int ring;  // h ring slots in scheduler rows; 0 = h holds every row
     int unmet_dependency;  // > 0 only in the failure-detection test: a wait nothing satisfies
     unsigned long long wait_ns;  // limit of every bounded wait
     unsigned epoch;
@@ -428,6 +439,17 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 const int brow = TN ? band0 + static_cast<int>(rank) *
                                                   (tile_tokens(c.offs[e + 1] - band0, kTileRows) >> 1)
                                     : 0;
+                // h rows of this scheduler row: slot (row mod Q) of the ring, or in place
+                const int hoff = p.ring ? (t.row % p.ring) * kTileRows - band0 : 0;
+                if (t.kind == 0 && p.ring && t.row >= p.ring) {
+                    // the slot's previous row must be read by all its Linear-2 tiles
+                    const unsigned long long tw = tr ? clock64() : 0;
+                    if (!wait_rows_ready(&p.l2_done[t.row - p.ring], static_cast<unsigned>(CG * p.P2),
+                                         abort_flag, p.status, 0x40000000u | static_cast<unsigned>(t.row),
+                                         p.wait_ns))
+                        break;
+                    if (tr) w_rows += clock64() - tw;
+                }
                 if (t.kind == 1) {
                     const unsigned long long tw = tr ? clock64() : 0;
                     if (!wait_rows_ready(&p.l1_done[t.row],
@@ -475,7 +497,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         } else {
                             tma_load_3d<CG>(&tm_w2, bar, a, kb * kBlockK,
                                             t.n * p.N2 + static_cast<int>(rank) * kBlockM, e);
-                            tma_load_2d<CG>(&tm_h, bar, b, kb * kBlockK, brow);
+                            tma_load_2d<CG>(&tm_h, bar, b, kb * kBlockK, brow + hoff);
                         }
                     } else if (t.kind == 0) {
                         tma_load_2d<CG>(&tm_x, bar, a, kb * kBlockK, row0);
@@ -485,7 +507,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                             tma_load_3d<CG>(&tm_w3, bar, CG == 1 ? b + kBTileBytes / 2 : b,
                                             kb * kBlockK, t.n * kL1N, e);
                     } else {
-                        tma_load_2d<CG>(&tm_h, bar, a, kb * kBlockK, row0);
+                        tma_load_2d<CG>(&tm_h, bar, a, kb * kBlockK, row0 + hoff);
                         tma_load_3d<CG>(&tm_w2, bar, b, kb * kBlockK,
                                         t.n * p.N2 + static_cast<int>(rank) * (p.N2 / CG), e);
                     }
@@ -683,7 +705,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const int half = lane & 1;
                         const int col = t.n * kL1N + static_cast<int>(rank) * (kL1N / 2) + (q & 1) * 32 +
                                         half * 16;
-                        const long hrow = static_cast<long>(band0) + ch * 32 + tk;
+                        const long hrow = static_cast<long>(band0) + ch * 32 + tk +
+                                          (p.ring ? (t.row % p.ring) * kTileRows - band0 : 0);
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {
                             const int j = jj ^ ((lane >> 2) & 1);  // spread the lanes over the banks
@@ -724,7 +747,12 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 // full 128-byte row segments per warp instruction.
                 uint8_t *stg = s_epi + (warp - 2) * kEpiStageBytes;
                 const int nchunks = t.kind == 0 ? kL1N / 64 : p.N2 / 64;
-                uint16_t *const out_base = t.kind == 0 ? p.h : p.y;
+                // h rows go to the row's ring slot when the ring is on
+                const long hoff = (t.kind == 0 && p.ring)
+                                      ? static_cast<long>(t.row % p.ring) * kTileRows -
+                                            (c.offs[e] + (t.row - c.row_start[e]) * kTileRows)
+                                      : 0;
+                uint16_t *const out_base = t.kind == 0 ? p.h + hoff * p.F : p.y;
                 const int out_ld = t.kind == 0 ? p.F : p.d;
                 const int col_base = t.kind == 0 ? t.n * kL1N : t.n * p.N2;
                 for (int ch = 0; ch < nchunks; ++ch) {
@@ -786,12 +814,14 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 if (rec) rec[7] = clock64();
                 if (stored) {
                     __threadfence();
-                    if (t.kind == 0)
+                    if (t.kind == 0) {
                         red_release_add_u32(&p.l1_done[t.row], 1u);
-                    else
+                    } else {
                         st_release_u32(
                             &p.l2_flags[(static_cast<long>(t.row) * p.P2 + t.n) * CG + rank],
                             p.epoch);
+                        if (p.ring) red_release_add_u32(&p.l2_done[t.row], 1u);
+                    }
                 }
             }
             __syncwarp();
@@ -925,18 +955,25 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
     // bound keeps the dependency waits deadlock-free.
     p.lead = a.lead > 0 ? a.lead : 2 * (p.group + (instances + p.P1 - 1) / p.P1) + 1;
     if (p.lead < p.group) p.lead = p.group;
+    if (p.ring) {
+        // a ring of Q rows bounds the lead: Q >= D + group + 1
+        if (p.ring < 2 * p.group + 1 || p.schedule != 0) return cudaErrorInvalidConfiguration;
+        if (p.lead > p.ring - p.group - 1) p.lead = p.ring - p.group - 1;
+    }
 
     const long R = a.R;
     CUtensorMap tx, th, tw1, tw3, tw2;
     if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, kBlockM) ||
-        !make_map_2d(&th, a.h, a.F, R, kBlockK, kBlockM) ||
+        !make_map_2d(&th, a.h, a.F, p.ring ? static_cast<long>(p.ring) * Cfg<CG>::kTileRows : R, kBlockK,
+                     kBlockM) ||
         !make_map_3d(&tw1, a.w1, a.d, a.F, a.E, kBlockK, TN ? kL1N / 2 : kL1N) ||
         !make_map_3d(&tw3, a.w3, a.d, a.F, a.E, kBlockK, TN ? kL1N / 2 : kL1N) ||
         !make_map_3d(&tw2, a.w2, a.F, a.d, a.E, kBlockK, TN ? kBlockM : p.N2 / CG))
         return cudaErrorInvalidValue;
 
     if (!a.counters_zeroed) {
-        cudaError_t err = cudaMemsetAsync(a.l1_done, 0, sizeof(unsigned) * a.max_rows, stream);
+        // l1_done and, right after it, l2_done
+        cudaError_t err = cudaMemsetAsync(a.l1_done, 0, 2 * sizeof(unsigned) * a.max_rows, stream);
         if (err != cudaSuccess) return err;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(instances * CG), 1, 1);
@@ -953,6 +990,8 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.h = a.h;
     p.y = a.y;
     p.l1_done = a.l1_done;
+    p.l2_done = a.l1_done + a.max_rows;
+    p.ring = a.h_ring_rows;
     p.l2_flags = a.l2_flags;
     p.status = a.status;
     p.E = a.E;

@@ -48,13 +48,14 @@ struct FfnArgs {
     const uint16_t *w2;      // [E,d,F]
     uint16_t *h;             // [R,F]
     uint16_t *y;             // [R,d]
-    unsigned *l1_done;       // [max_rows]
+    unsigned *l1_done;       // [2 * max_rows]: Linear-1 counters, then Linear-2 counters
     unsigned *l2_flags;      // [max_rows * P2]
     unsigned *status;        // 4 words
     long max_rows;
     int R, d, F, E;
     int schedule, lead, num_ctas, l2_block_n, group_rows, cta_group;
     int orientation;  // 0 = choose, 1 = tokens on the MMA's M side, 2 = on its N side
+    int h_ring_rows;  // h ring slots in scheduler rows (0 = h holds every row)
     int wait_limit_us, unmet_dependency;
     unsigned long long *trace;  // optional per-CTA counters (16 per CTA)
     unsigned long long *tile_trace;  // optional per-tile timeline (8 words per tile)

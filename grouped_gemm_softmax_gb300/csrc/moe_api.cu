@@ -74,7 +74,7 @@ moe_status_t check_shape(const moe_shape_t *s)
     return MOE_OK;
 }
 
-Layout make_layout(const moe_shape_t *s)
+Layout make_layout(const moe_shape_t *s, const moe_tuning_t *t = nullptr)
 {
     Layout L{};
     const size_t T = s->T, d = s->d, E = s->E, k = s->top_k, F = s->ffn;
@@ -91,17 +91,21 @@ Layout make_layout(const moe_shape_t *s)
     L.bytes[MOE_WS_ROW_OF_SLOT] = R * 4;
     L.bytes[MOE_WS_SLOT_OF_ROW] = R * 4;
     L.bytes[MOE_WS_X_PERM] = R * d * 2;
-    L.bytes[MOE_WS_H] = R * F * 2;
+    const size_t ring = t ? static_cast<size_t>(t->h_ring_rows) : 0;
+    L.bytes[MOE_WS_H] = ring ? ring * 256 * F * 2 : R * F * 2;
     L.bytes[MOE_WS_Y_PERM] = R * d * 2;
     L.bytes[MOE_WS_CHUNK_BASE] = chunks * E * 4;
-    L.bytes[MOE_WS_L1_DONE] = static_cast<size_t>(L.max_rows) * 4;
+    L.bytes[MOE_WS_L1_DONE] = static_cast<size_t>(L.max_rows) * 8;  // Linear-1 then Linear-2 counts
     L.bytes[MOE_WS_L2_FLAGS] = static_cast<size_t>(L.max_rows) * p2max * 4;
+    // h last: the other regions keep their offsets whatever h's size
     size_t off = 0;
     for (int i = 0; i < MOE_WS_NUM_REGIONS; ++i) {
+        if (i == MOE_WS_H) continue;
         L.off[i] = off;
         off = align_up(off + L.bytes[i]);
     }
-    L.total = off;
+    L.off[MOE_WS_H] = off;
+    L.total = align_up(off + L.bytes[MOE_WS_H]);
     return L;
 }
 
@@ -139,6 +143,8 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->orientation < 0 || t->orientation > 2) return MOE_ERR_INVALID_ARG;
     if (t->orientation == 2 && t->cta_group == 1) return MOE_ERR_INVALID_ARG;
     if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
+    if (t->h_ring_rows < 0 || (t->h_ring_rows > 0 && t->schedule != MOE_SCHEDULE_INTERLEAVED))
+        return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -170,6 +176,7 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.group_rows = tune ? tune->group_rows : 0;
     a.cta_group = tune ? tune->cta_group : 0;
     a.orientation = tune ? tune->orientation : 0;
+    a.h_ring_rows = tune ? tune->h_ring_rows : 0;
     a.wait_limit_us = tune ? tune->wait_limit_us : 0;
     a.unmet_dependency = tune ? tune->unmet_dependency : 0;
     a.trace = tune ? static_cast<unsigned long long *>(tune->trace) : nullptr;
@@ -178,7 +185,10 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.counters_zeroed = counters_zeroed;
     a.epoch = next_epoch();
     if (moe::encode_tiled_fn() == nullptr) return MOE_ERR_CUDA;
-    return cuda_status(moe::launch_ffn(a, stream));
+    const cudaError_t err = moe::launch_ffn(a, stream);
+    // a ring too small for the raster group is a configuration the caller chose
+    if (err == cudaErrorInvalidConfiguration && a.h_ring_rows > 0) return MOE_ERR_INVALID_ARG;
+    return cuda_status(err);
 }
 
 }  // namespace
@@ -202,6 +212,26 @@ size_t moe_workspace_bytes(const moe_shape_t *shape)
 {
     if (check_shape(shape) != MOE_OK) return 0;
     return make_layout(shape).total;
+}
+
+size_t moe_workspace_bytes_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning)
+{
+    if (check_shape(shape) != MOE_OK || check_tuning(tuning) != MOE_OK) return 0;
+    return make_layout(shape, tuning).total;
+}
+
+moe_status_t moe_workspace_region_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,
+                                        int r, size_t *offset, size_t *bytes)
+{
+    moe_status_t st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if ((st = check_tuning(tuning)) != MOE_OK) return st;
+    if (r < 0 || r >= MOE_WS_NUM_REGIONS || offset == nullptr || bytes == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    const Layout L = make_layout(shape, tuning);
+    *offset = L.off[r];
+    *bytes = L.bytes[r];
+    return MOE_OK;
 }
 
 moe_status_t moe_workspace_region(const moe_shape_t *shape, int r, size_t *offset, size_t *bytes)
@@ -241,7 +271,7 @@ moe_status_t moe_dispatch(const moe_shape_t *shape, const moe_bf16_t *x, const i
     if (st != MOE_OK) return st;
     if (!expert_counts || !expert_offsets || !ws) return MOE_ERR_INVALID_ARG;
     const Layout L = make_layout(shape);
-    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < L.off[MOE_WS_H]) return MOE_ERR_WORKSPACE;  // every region it uses lies before h
     if (shape->T > 0 && (!x || !topk_idx || !row_of_slot || !slot_of_row || !x_perm))
         return MOE_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm)) || !aligned16(ws) ||
@@ -278,7 +308,7 @@ moe_status_t moe_expert_ffn_tuned(const moe_shape_t *shape, const moe_tuning_t *
     if (st != MOE_OK) return st;
     if ((st = check_tuning(tuning)) != MOE_OK) return st;
     if (!ws) return MOE_ERR_INVALID_ARG;
-    const Layout L = make_layout(shape);
+    const Layout L = make_layout(shape, tuning);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     if (shape->T == 0) return MOE_OK;
     if (!x_perm || !expert_offsets || !W1 || !W3 || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
@@ -333,7 +363,7 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     if (st != MOE_OK) return st;
     if ((st = check_tuning(tuning)) != MOE_OK) return st;
     if (!ws) return MOE_ERR_INVALID_ARG;
-    const Layout L = make_layout(shape);
+    const Layout L = make_layout(shape, tuning);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     if (shape->T == 0) return MOE_OK;
     if (!x || !w_router || !W1 || !W3 || !W2 || !out_segments) return MOE_ERR_INVALID_ARG;
@@ -372,7 +402,7 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     da.chunk_base = region<int32_t>(ws, L, MOE_WS_CHUNK_BASE);
     da.status = region<unsigned>(ws, L, MOE_WS_STATUS);
     da.zero_words = region<unsigned>(ws, L, MOE_WS_L1_DONE);
-    da.zero_count = L.max_rows;
+    da.zero_count = 2 * L.max_rows;  // Linear-1 and Linear-2 row counters
     da.T = shape->T;
     da.d = shape->d;
     da.E = shape->E;

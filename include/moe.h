@@ -109,6 +109,15 @@ typedef struct {
                            NULL = off */
     int tile_trace_cap; /* tiles recorded per CTA (later tiles are not recorded) */
     int orientation;    /* moe_orientation_t: which MMA operand holds the tokens; 0 = default */
+    int h_ring_rows;    /* 0 = h holds all R rows; Q > 0 = h is a ring of Q scheduler rows
+                           (Xian et al., Algorithm 1, "destination ring slot"): row p lives in
+                           slot p mod Q and a Linear-1 tile of row p >= Q waits (bounded)
+                           until every Linear-2 tile of row p - Q has finished. Q must be at
+                           least 2 * raster group + 1 scheduler rows (33 with the defaults)
+                           and the lead is lowered to Q - group - 1 if above it, which keeps
+                           the waits deadlock-free; interleaved schedule only (else
+                           MOE_ERR_INVALID_ARG). The workspace must then come from
+                           moe_workspace_bytes_tuned with the same tuning. */
 } moe_tuning_t;
 
 /* Human-readable name of a status code. Never NULL. */
@@ -117,6 +126,11 @@ const char *moe_status_string(moe_status_t status);
 /* Bytes of device workspace that moe_layer_forward needs for this shape (a
  * superset of what moe_dispatch and moe_expert_ffn need). 0 for an invalid shape. */
 size_t moe_workspace_bytes(const moe_shape_t *shape);
+
+/* The same for a tuning (NULL = defaults): with h_ring_rows = Q > 0 the h
+ * region is Q x 256 x F bf16 instead of R x F. The h region is the last in the
+ * workspace, so every other region has the same offset in both layouts. */
+size_t moe_workspace_bytes_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning);
 
 /* Byte offset and size of one named region inside the workspace (for
  * inspection: routing results, the permuted rows, h, y_perm, flags).
@@ -130,15 +144,20 @@ enum {
     MOE_WS_ROW_OF_SLOT = 5, /* [R] int32 */
     MOE_WS_SLOT_OF_ROW = 6, /* [R] int32 */
     MOE_WS_X_PERM = 7,      /* [R,d] bf16 */
-    MOE_WS_H = 8,           /* [R,F] bf16: SwiGLU activations */
+    MOE_WS_H = 8,           /* [R,F] bf16: SwiGLU activations (a ring of Q x 256 rows with
+                               h_ring_rows = Q); placed last in the workspace */
     MOE_WS_Y_PERM = 9,      /* [R,d] bf16 */
     MOE_WS_CHUNK_BASE = 10, /* dispatch scratch: [chunks,E] int32 */
-    MOE_WS_L1_DONE = 11,    /* per scheduler row: finished Linear-1 tiles, u32 */
+    MOE_WS_L1_DONE = 11,    /* per scheduler row: finished Linear-1 tiles, u32; then per row the
+                               finished Linear-2 tiles (used by the h ring) */
     MOE_WS_L2_FLAGS = 12,   /* per Linear-2 tile: ready flag = epoch of the call that wrote it, u32 */
     MOE_WS_NUM_REGIONS = 13
 };
 moe_status_t moe_workspace_region(const moe_shape_t *shape, int region, size_t *offset,
                                   size_t *bytes);
+/* The same for the layout of moe_workspace_bytes_tuned(shape, tuning). */
+moe_status_t moe_workspace_region_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,
+                                        int region, size_t *offset, size_t *bytes);
 
 /* Step 1, routing (Cui et al. section 2.1 step 1; Xian et al. section 2.2).
  *   z[t,e] = sum_i x[t,i] * w_router[e,i] (+ expert_bias[e]), accumulated in
@@ -155,8 +174,9 @@ moe_status_t moe_route(const moe_shape_t *shape, const moe_bf16_t *x, const moe_
  *   expert_counts[e] = #{(t,j): topk_idx[t,j] == e}; expert_offsets = exclusive
  *   scan (E+1 entries, last = R); row_of_slot[t*k+j] = destination row;
  *   slot_of_row = its inverse; x_perm[r] = x[slot_of_row[r] / k].
- * x [T,d] bf16, topk_idx [T,k] int32, outputs as named; ws: at least
- * moe_workspace_bytes(shape) bytes (uses the CHUNK_BASE and STATUS regions).
+ * x [T,d] bf16, topk_idx [T,k] int32, outputs as named; ws: a workspace of
+ * moe_workspace_bytes or moe_workspace_bytes_tuned (uses the CHUNK_BASE and
+ * STATUS regions, which lie before h; ws_bytes must reach the start of h).
  * An expert id outside [0,E) is skipped (its row_of_slot entry becomes -1, it
  * is not counted) and recorded as MOE_ERR_INVALID_ARG in the device status. */
 moe_status_t moe_dispatch(const moe_shape_t *shape, const moe_bf16_t *x, const int32_t *topk_idx,
@@ -205,7 +225,8 @@ moe_status_t moe_expert_ffn(const moe_shape_t *shape, const moe_bf16_t *x_perm,
                             const moe_bf16_t *W3, const moe_bf16_t *W2, moe_bf16_t *y_perm,
                             void *ws, size_t ws_bytes, moe_stream_t stream);
 
-/* moe_expert_ffn with an explicit tile schedule (tuning may be NULL = defaults). */
+/* moe_expert_ffn with an explicit tile schedule (tuning may be NULL = defaults);
+ * ws_bytes is checked against moe_workspace_bytes_tuned(shape, tuning). */
 moe_status_t moe_expert_ffn_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,
                                   const moe_bf16_t *x_perm, const int32_t *expert_offsets,
                                   const moe_bf16_t *W1, const moe_bf16_t *W3, const moe_bf16_t *W2,
@@ -230,7 +251,8 @@ moe_status_t moe_layer_forward(const moe_shape_t *shape, const moe_bf16_t *x,
                                moe_bf16_t *const *out_segments, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
-/* moe_layer_forward with an explicit tile schedule (tuning may be NULL). */
+/* moe_layer_forward with an explicit tile schedule (tuning may be NULL); the
+ * workspace is sized by moe_workspace_bytes_tuned(shape, tuning). */
 moe_status_t moe_layer_forward_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,
                                      const moe_bf16_t *x, const moe_bf16_t *w_router,
                                      const float *expert_bias, const moe_bf16_t *W1,

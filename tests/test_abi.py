@@ -131,3 +131,32 @@ def test_binding_rejects_wrong_tensors_before_the_library():
     with pytest.raises(ValueError):  # CPU tensors are refused: no host fallback exists
         moe.route(s, torch.zeros(4, 8, dtype=torch.bfloat16), torch.zeros(2, 8, dtype=torch.bfloat16),
                   None, torch.zeros(4, dtype=torch.int32), torch.zeros(4))
+
+
+def test_h_ring_workspace_layout_and_checks(lib):
+    """An h ring shrinks only the h region, which is the last one: every other
+    region keeps its offset, so moe_dispatch accepts either workspace. A ring
+    needs the interleaved schedule."""
+    s = moe.Shape(T=4096, d=2048, E=64, top_k=6, ffn=1408)
+    ring = moe.Tuning(h_ring_rows=40)
+    full_nb, ring_nb = moe.workspace_bytes(s), moe.workspace_bytes(s, ring)
+    assert ring_nb < full_nb
+    for r in range(13):
+        off_f, nb_f = moe.workspace_region(s, r)
+        off_r, nb_r = moe.workspace_region(s, r, ring)
+        assert off_f == off_r
+        if r == moe.WS.H:
+            assert nb_r == 40 * 256 * 1408 * 2 and off_r + nb_r <= ring_nb
+        else:
+            assert nb_f == nb_r and off_r + nb_r <= moe.workspace_region(s, moe.WS.H)[0]
+    c = ctypes.byref(s.c())
+    for bad in (moe.Tuning(h_ring_rows=40, schedule=moe.SCHEDULE_EXPERT_WAVE), moe.Tuning(h_ring_rows=-1)):
+        assert lib.moe_workspace_bytes_tuned(c, ctypes.byref(bad.c())) == 0
+    fake = ctypes.c_void_p(1 << 20)
+    bad = moe.Tuning(h_ring_rows=40, schedule=moe.SCHEDULE_EXPERT_WAVE)
+    assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad.c()), fake, fake, fake, fake, fake, fake,
+                                    fake, full_nb, None) == moe.MOE_ERR_INVALID_ARG
+    # the untuned FFN needs the full workspace; a ring-sized one is refused
+    assert lib.moe_expert_ffn(c, fake, fake, fake, fake, fake, fake, fake, ring_nb, None) == \
+        moe.MOE_ERR_WORKSPACE
+

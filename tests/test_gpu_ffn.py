@@ -38,7 +38,8 @@ def run_ffn(c, tuning=None, ws=None):
     moe.expert_ffn(s, c["x"], off, c["w1"], c["w3"], c["w2"], y, ws, tuning=tuning)
     st = moe.last_device_status(ws)
     assert st == moe.MOE_OK, (st, moe.last_device_detail())
-    h = moe.ws_view(ws, s, moe.WS.H, torch.bfloat16, (c["R"], c["F"])).clone()
+    ring = tuning is not None and tuning.h_ring_rows > 0  # then h holds only the last rows
+    h = None if ring else moe.ws_view(ws, s, moe.WS.H, torch.bfloat16, (c["R"], c["F"])).clone()
     return s, ws, h, y
 
 
@@ -135,6 +136,40 @@ def test_default_orientation_puts_tokens_on_n_for_small_experts():
     _, _, hd, yd = run_ffn(c)
     _, _, hn, yn = run_ffn(c, tuning=moe.Tuning(orientation=moe.ORIENT_TOKENS_N))
     assert torch.equal(yd.view(torch.int16), yn.view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", sorted(MODES))
+def test_h_ring_is_bit_identical_to_full_h(mode):
+    """h as a ring of Q scheduler rows (Linear-1 of row p waits for the
+    Linear-2 tiles of row p - Q): the same bits as with every row in place,
+    for the smallest ring the raster group allows and a larger one, with many
+    wrap-arounds."""
+    need_gpu()
+    c = make_case([70, 0, 129, 1, 255, 57, 300, 12] * 8, 256, 384, seed=13)
+    base = dict(MODES[mode], group_rows=4)
+    _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(**base))
+    group = 4 // MODES[mode]["cta_group"]  # raster group in scheduler rows
+    for ring in (2 * group + 1, 12):
+        t = moe.Tuning(**base, h_ring_rows=ring)
+        s = moe.Shape(T=c["R"], d=c["d"], E=c["E"], top_k=1, ffn=c["F"])
+        ws = moe.alloc_workspace(s, tuning=t)
+        assert ws.numel() < moe.workspace_bytes(s)
+        _, _, _, y = run_ffn(c, tuning=t, ws=ws)
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16)), ring
+
+
+def test_h_ring_below_the_deadlock_free_size_is_refused():
+    need_gpu()
+    c = make_case([300, 200], 256, 256, seed=14)
+    s = moe.Shape(T=c["R"], d=c["d"], E=c["E"], top_k=1, ffn=c["F"])
+    t = moe.Tuning(h_ring_rows=8)  # default raster group: 16 pair rows -> needs >= 33
+    ws = moe.alloc_workspace(s, tuning=t)
+    y = torch.zeros(c["R"], c["d"], dtype=torch.bfloat16, device="cuda")
+    off = torch.from_numpy(c["offsets"]).cuda()
+    with pytest.raises(moe.MoEError) as e:
+        moe.expert_ffn(s, c["x"], off, c["w1"], c["w3"], c["w2"], y, ws, tuning=t)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    assert torch.all(y == 0)
 
 
 @pytest.mark.parametrize("n2", [64, 128, 192, 256])

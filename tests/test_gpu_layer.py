@@ -104,6 +104,19 @@ def test_schedules_and_repeat_calls_are_bit_identical():
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 
 
+def test_layer_with_h_ring_is_bit_identical():
+    need_gpu()
+    cfg = synth.CONFIGS["tiny"]
+    layer = GpuLayer(cfg)
+    a = layer.forward().clone()
+    t = moe.Tuning(h_ring_rows=33)
+    ws = moe.alloc_workspace(layer.shape, tuning=t)
+    i = layer.inp
+    moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=t)
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), a.view(torch.int16))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mid", "dit", "fine", "coarse"])
 def test_full_size_configs(name):
