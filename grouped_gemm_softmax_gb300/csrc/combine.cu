@@ -55,8 +55,9 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ gate,
     float g[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-        src[j] = j < k ? reinterpret_cast<const uint4 *>(y + static_cast<long>(row_of_slot[t * k + j]) * d)
-                       : nullptr;
+        // a slot whose expert id was out of range has no row (-1): no term
+        const int r = j < k ? row_of_slot[t * k + j] : -1;
+        src[j] = r >= 0 ? reinterpret_cast<const uint4 *>(y + static_cast<long>(r) * d) : nullptr;
         g[j] = j < k ? gate[t * k + j] : 0.0f;
     }
     uint4 *dst = reinterpret_cast<uint4 *>(seg.p[t / rows_per_seg] + (t % rows_per_seg) * static_cast<long>(d));
@@ -67,14 +68,14 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ gate,
         for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (j < k && v0 + 32 * u < nvec) val[u][j] = src[j][v0 + 32 * u];
+                if (src[j] != nullptr && v0 + 32 * u < nvec) val[u][j] = src[j][v0 + 32 * u];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (v0 + 32 * u >= nvec) break;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (j < k) acc_bf16x8(acc, val[u][j], g[j]);
+                if (src[j] != nullptr) acc_bf16x8(acc, val[u][j], g[j]);
             uint4 o;
             o.x = pack2(acc[0], acc[1]);
             o.y = pack2(acc[2], acc[3]);

@@ -25,6 +25,16 @@
 // sequence (an instance emits all its Linear-2 tiles of row r before any
 // Linear-1 tile past row r + D), so these waits cannot deadlock either.
 //
+// Fused combine (FC; Cui et al., section 3.3: a consumer polls the producer's
+// per-tile signals and sends each finished block to its owner): two more warps
+// per CTA consume scheduler rows as their Linear-2 tiles finish (the per-row
+// Linear-2 counter reaches CTAs per tile * P2). A token is combined by the
+// unit that holds its last row (in scheduler-row order) once its other rows'
+// rows are finished too, and written to its owner segment; the epilogue warps
+// join after their last tile. The consumers wait only on Linear-2 tiles, which
+// never wait on them, and the fp32 sum runs in j order exactly as the combine
+// kernel's, so the output bits are the same.
+//
 // Order (Xian et al., Algorithm 1, read for unpaired CTAs): CTA g of G walks two
 // cursors k1, k2 (start g, step G) over the Linear-1 and Linear-2 tile streams
 // (row-major over (row, n)); it emits the Linear-2 tile at k2 when its row
@@ -80,6 +90,7 @@ constexpr int kDefaultGroupRows = 32;  // raster group, in 128-row M-tiles
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr int kThreads = 192;
+constexpr int kConsumerThreads = 64;  // two consumer warps with the fused combine
 constexpr int kEpiThreads = 128;
 constexpr int kTraceWords = 16;  // per-CTA counters when tracing is on
 // per-tile timeline record (clock64 of the CTA's SM):
@@ -109,6 +120,12 @@ struct GemmParams {
     int kb1, kb2;
     int schedule, lead, group, cg;
     int ring;  // h ring slots in scheduler rows; 0 = h holds every row
+    int fc;    // fused combine: count finished Linear-2 tiles per row for the consumers
+    const float *gate;
+    const int32_t *row_of_slot;
+    const int32_t *slot_of_row;
+    int T, k, rows_per_seg;
+    uint16_t *seg[kMaxSegments];
     int unmet_dependency;  // > 0 only in the failure-detection test: a wait nothing satisfies
     unsigned long long wait_ns;  // limit of every bounded wait
     unsigned epoch;
@@ -127,6 +144,7 @@ struct SmemCtl {
     uint32_t tmem_base;
     int abort;
     int epi_fail;  // TN epilogue: a warp gave up (the warp pairs meet at barriers)
+    int cunit;     // fused combine: next consumer unit of this CTA
     int nwaves;
     int offs[kMaxExperts + 1];       // expert row offsets (copy of expert_offsets)
     int row_start[kMaxExperts + 1];  // first scheduler row of each expert
@@ -251,7 +269,8 @@ struct Scheduler {
 
 __device__ __forceinline__ bool wait_rows_ready(const unsigned *ctr, unsigned target,
                                                 volatile int *cta_abort, unsigned *status,
-                                                unsigned detail, unsigned long long limit_ns)
+                                                unsigned detail, unsigned long long limit_ns,
+                                                unsigned where = kWhereProducerDep)
 {
     if (ld_acquire_u32(ctr) >= target) return true;
     const unsigned long long t0 = globaltimer_ns();
@@ -265,7 +284,7 @@ __device__ __forceinline__ bool wait_rows_ready(const unsigned *ctr, unsigned ta
                 return false;
             }
             if (globaltimer_ns() - t0 > limit_ns) {
-                report_failure(status, kStatusTimeout, kWhereProducerDep, detail);
+                report_failure(status, kStatusTimeout, where, detail);
                 *cta_abort = 1;
                 return false;
             }
@@ -296,8 +315,132 @@ __device__ __forceinline__ int tile_tokens(int remaining, int rows)
     return (min(remaining, rows) + 15) & ~15;
 }
 
-template <int CG, bool TN>
-__global__ void __launch_bounds__(kThreads, 1)
+// last index i in [0, n) with v[i] <= x (v non-decreasing, v[0] <= x)
+__device__ __forceinline__ int last_le(const int *v, int n, int x)
+{
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (v[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Fused combine, run by one warp: take this CTA's units from a shared counter
+// (unit U = 32 rows of scheduler row U / units-per-row; CTA g owns U = g,
+// g + gridDim.x, ... in increasing U, so every scheduler row's rows are spread
+// over many CTAs), wait until the unit's row has all its Linear-2 tiles
+// finished, and combine every token whose last row lies in the unit. False
+// when a wait gave up.
+template <int CG>
+__device__ bool combine_consumer(SmemCtl &c, const GemmParams &p, int lane, volatile int *abort_flag)
+{
+    constexpr int kTileRows = Cfg<CG>::kTileRows;
+    constexpr int kUnits = kTileRows / 32;
+    const int E = p.E;
+    const int P = c.row_start[E];
+    const int total = P * kUnits;
+    const int mine = total > static_cast<int>(blockIdx.x)
+                         ? (total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                               static_cast<int>(gridDim.x)
+                         : 0;
+    const unsigned target = static_cast<unsigned>(CG * p.P2);
+    const int nvec = p.d / 8;
+    for (;;) {
+        int u = 0;
+        if (lane == 0) u = atomicAdd(&c.cunit, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (u >= mine) return true;
+        const int U = static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x);
+        const int b = U / kUnits;
+        const int e = last_le(c.row_start, E, b);
+        const int band0 = c.offs[e] + (b - c.row_start[e]) * kTileRows;
+        const int r0 = band0 + (U % kUnits) * 32;
+        const int r1 = min(c.offs[e + 1], band0 + kTileRows);
+        if (r0 >= r1) continue;
+        bool ok = true;
+        if (lane == 0)
+            ok = wait_rows_ready(&p.l2_done[b], target, abort_flag, p.status,
+                                 0x20000000u | static_cast<unsigned>(b), p.wait_ns, kWhereCombine);
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
+        __syncwarp();
+        // lane i looks at row r0 + i: its token, the token's rows and their
+        // scheduler rows; the token belongs here if b is the last of them
+        const int r = r0 + lane;
+        int t = 0, rows[kMaxTopK], rb[kMaxTopK];
+        bool own = false;
+        if (r < r1) {
+            t = __ldg(p.slot_of_row + r) / p.k;
+            int bmax = -1;
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                rows[j] = j < p.k ? __ldg(p.row_of_slot + static_cast<long>(t) * p.k + j) : -1;
+                rb[j] = -1;
+                if (rows[j] >= 0) {  // a slot without a row (bad expert id) adds no term
+                    const int ej = last_le(c.offs, E, rows[j]);
+                    rb[j] = c.row_start[ej] + (rows[j] - c.offs[ej]) / kTileRows;
+                    bmax = max(bmax, rb[j]);
+                }
+            }
+            own = bmax == b;
+        }
+        unsigned todo = __ballot_sync(0xffffffffu, own);
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int tt = __shfl_sync(0xffffffffu, t, src);
+            // the token's other rows must be finished as well
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                const int bj = __shfl_sync(0xffffffffu, rb[j], src);
+                if (bj >= 0 && bj != b) {
+                    bool okj = true;
+                    if (lane == 0)
+                        okj = wait_rows_ready(&p.l2_done[bj], target, abort_flag, p.status,
+                                              0x20000000u | static_cast<unsigned>(bj), p.wait_ns,
+                                              kWhereCombine);
+                    if (!__shfl_sync(0xffffffffu, okj ? 1 : 0, 0)) return false;
+                }
+            }
+            __syncwarp();
+            const uint4 *src_rows[kMaxTopK];
+            float g[kMaxTopK];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                const int rj = __shfl_sync(0xffffffffu, rows[j], src);
+                src_rows[j] = rj >= 0 ? reinterpret_cast<const uint4 *>(p.y + static_cast<long>(rj) * p.d)
+                                      : nullptr;
+                g[j] = j < p.k ? __ldg(p.gate + static_cast<long>(tt) * p.k + j) : 0.0f;
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(p.seg[tt / p.rows_per_seg] +
+                                                   static_cast<long>(tt % p.rows_per_seg) * p.d);
+            for (int v = lane; v < nvec; v += 32) {
+                uint4 val[kMaxTopK];
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j)
+                    if (src_rows[j] != nullptr) val[j] = src_rows[j][v];
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j) {
+                    if (src_rows[j] != nullptr) {
+                        const uint32_t w[4] = {val[j].x, val[j].y, val[j].z, val[j].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            acc[2 * h] = fmaf(g[j], __uint_as_float(w[h] << 16), acc[2 * h]);
+                            acc[2 * h + 1] = fmaf(g[j], __uint_as_float(w[h] & 0xFFFF0000u), acc[2 * h + 1]);
+                        }
+                    }
+                }
+                dst[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+            }
+        }
+    }
+}
+
+template <int CG, bool TN, bool FC>
+__global__ void __launch_bounds__(FC ? kThreads + kConsumerThreads : kThreads, 1)
 grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_h,
                            const __grid_constant__ CUtensorMap tm_w1,
@@ -334,6 +477,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         mbar_init(&c.drain, 1);
         c.abort = 0;
         c.epi_fail = 0;
+        c.cunit = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -606,6 +750,9 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 o[5] = clock64() - t0;
             }
         }
+    } else if (FC && warp >= kThreads / 32) {
+        // ------------------------------------------------------------ combine consumers
+        combine_consumer<CG>(c, p, lane, abort_flag);
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
@@ -820,12 +967,16 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         st_release_u32(
                             &p.l2_flags[(static_cast<long>(t.row) * p.P2 + t.n) * CG + rank],
                             p.epoch);
-                        if (p.ring) red_release_add_u32(&p.l2_done[t.row], 1u);
+                        if (p.ring || p.fc) red_release_add_u32(&p.l2_done[t.row], 1u);
                     }
                 }
             }
             __syncwarp();
         }
+        // with the fused combine, the epilogue warps turn consumers once their
+        // tiles are done (unless a wait gave up)
+        if constexpr (FC)
+            if (!*abort_flag && ld_volatile_u32(p.status) == 0u) combine_consumer<CG>(c, p, lane, abort_flag);
         if (tr && publisher) {
             unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
             o[6] = w_full;
@@ -908,7 +1059,7 @@ long ffn_max_rows(long R, int E)
 
 namespace {
 
-template <int CG, bool TN>
+template <int CG, bool TN, bool FC>
 cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
 {
     constexpr size_t smem = smem_bytes<CG>();
@@ -922,13 +1073,13 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(FC ? kThreads + kConsumerThreads : kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel<CG, TN>,
+        cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel<CG, TN, FC>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
         if (err != cudaSuccess) return err;
@@ -936,7 +1087,7 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
         // Linear-2 tiles wait on Linear-1 tiles of other CTAs)
         int clusters = 0;
         cfg.gridDim = dim3(static_cast<unsigned>(sms / CG * CG), 1, 1);
-        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG, TN>, &cfg);
+        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG, TN, FC>, &cfg);
         if (err != cudaSuccess) return err;
         max_instances = clusters < sms / CG ? clusters : sms / CG;
         if (max_instances <= 0) return cudaErrorInvalidConfiguration;
@@ -977,7 +1128,7 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
         if (err != cudaSuccess) return err;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(instances * CG), 1, 1);
-    return cudaLaunchKernelEx(&cfg, grouped_swiglu_gemm_kernel<CG, TN>, tx, th, tw1, tw3, tw2, p);
+    return cudaLaunchKernelEx(&cfg, grouped_swiglu_gemm_kernel<CG, TN, FC>, tx, th, tw1, tw3, tw2, p);
 }
 
 }  // namespace
@@ -1032,9 +1183,22 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.unmet_dependency = a.unmet_dependency > 0 ? 1 : 0;
     const int group = a.group_rows > 0 ? a.group_rows : kDefaultGroupRows;  // 128-row M-tiles
     p.group = (group + p.cg - 1) / p.cg;                                     // scheduler rows
-    if (tn) return launch_cg<2, true>(a, p, stream);
-    if (p.cg == 1) return launch_cg<1, false>(a, p, stream);
-    return launch_cg<2, false>(a, p, stream);
+    p.fc = a.gate != nullptr ? 1 : 0;
+    if (p.fc) {
+        p.gate = a.gate;
+        p.row_of_slot = a.row_of_slot;
+        p.slot_of_row = a.slot_of_row;
+        p.T = a.T;
+        p.k = a.k;
+        p.rows_per_seg = a.T / a.S;
+        for (int i = 0; i < kMaxSegments; ++i) p.seg[i] = i < a.S ? a.seg[i] : nullptr;
+        if (tn) return launch_cg<2, true, true>(a, p, stream);
+        if (p.cg == 1) return launch_cg<1, false, true>(a, p, stream);
+        return launch_cg<2, false, true>(a, p, stream);
+    }
+    if (tn) return launch_cg<2, true, false>(a, p, stream);
+    if (p.cg == 1) return launch_cg<1, false, false>(a, p, stream);
+    return launch_cg<2, false, false>(a, p, stream);
 }
 
 }  // namespace moe

@@ -56,6 +56,12 @@ struct FfnArgs {
     int schedule, lead, num_ctas, l2_block_n, group_rows, cta_group;
     int orientation;  // 0 = choose, 1 = tokens on the MMA's M side, 2 = on its N side
     int h_ring_rows;  // h ring slots in scheduler rows (0 = h holds every row)
+    // fused combine (consumer warps in the GEMM kernel); gate == nullptr = off
+    const float *gate;            // [T,k]
+    const int32_t *row_of_slot;   // [R]
+    const int32_t *slot_of_row;   // [R]
+    uint16_t *seg[kMaxSegments];  // S segments of [T/S, d]
+    int T, k, S;
     int wait_limit_us, unmet_dependency;
     unsigned long long *trace;  // optional per-CTA counters (16 per CTA)
     unsigned long long *tile_trace;  // optional per-tile timeline (8 words per tile)

@@ -145,15 +145,26 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
     if (t->h_ring_rows < 0 || (t->h_ring_rows > 0 && t->schedule != MOE_SCHEDULE_INTERLEAVED))
         return MOE_ERR_INVALID_ARG;
+    if (t->fused_combine < 0 || t->fused_combine > 1) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
 moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const Layout &L,
                          const moe_bf16_t *x_perm, const int32_t *offsets, const moe_bf16_t *W1,
                          const moe_bf16_t *W3, const moe_bf16_t *W2, moe_bf16_t *y_perm, void *ws,
-                         bool counters_zeroed, cudaStream_t stream)
+                         bool counters_zeroed, cudaStream_t stream,
+                         const moe::CombineArgs *fused = nullptr)
 {
     moe::FfnArgs a{};
+    if (fused != nullptr) {
+        a.gate = fused->gate;
+        a.row_of_slot = fused->row_of_slot;
+        a.slot_of_row = region<int32_t>(ws, L, MOE_WS_SLOT_OF_ROW);
+        for (int i = 0; i < kMaxSegments; ++i) a.seg[i] = fused->seg[i];
+        a.T = fused->T;
+        a.k = fused->k;
+        a.S = fused->S;
+    }
     a.x_perm = x_perm;
     a.offsets = offsets;
     a.w1 = W1;
@@ -312,6 +323,7 @@ moe_status_t moe_expert_ffn_tuned(const moe_shape_t *shape, const moe_tuning_t *
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     if (shape->T == 0) return MOE_OK;
     if (!x_perm || !expert_offsets || !W1 || !W3 || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (tuning && tuning->fused_combine) return MOE_ERR_INVALID_ARG;  // needs the layer's routing
     if (!aligned16(x_perm) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) ||
         !aligned16(y_perm) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
         return MOE_ERR_INVALID_ARG;
@@ -411,11 +423,6 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     err = moe::launch_dispatch(da, s);
     if (err != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
 
-    st = enqueue_ffn(shape, tuning, L, da.x_perm, da.offsets, W1, W3, W2,
-                     region<uint16_t>(ws, L, MOE_WS_Y_PERM), ws, true, s);
-    if (st != MOE_OK) return st;
-    if (!mark(3)) return MOE_ERR_CUDA;
-
     moe::CombineArgs ca{};
     for (int i = 0; i < shape->num_segments; ++i) ca.seg[i] = out_segments[i];
     ca.y = region<uint16_t>(ws, L, MOE_WS_Y_PERM);
@@ -425,8 +432,16 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     ca.d = shape->d;
     ca.k = shape->top_k;
     ca.S = shape->num_segments;
-    err = moe::launch_combine(ca, s);
-    if (err != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
+    const bool fused = tuning && tuning->fused_combine;
+    st = enqueue_ffn(shape, tuning, L, da.x_perm, da.offsets, W1, W3, W2,
+                     region<uint16_t>(ws, L, MOE_WS_Y_PERM), ws, true, s, fused ? &ca : nullptr);
+    if (st != MOE_OK) return st;
+    if (!mark(3)) return MOE_ERR_CUDA;
+    if (!fused) {
+        err = moe::launch_combine(ca, s);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (!mark(4)) return MOE_ERR_CUDA;
     return MOE_OK;
 }
 

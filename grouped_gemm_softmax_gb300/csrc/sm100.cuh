@@ -17,7 +17,7 @@ namespace moe {
 enum : unsigned { kStatusBadExpert = 1u, kStatusBadOffsets = 1u, kStatusTimeout = 5u };
 enum : unsigned {
     kWhereProducerEmpty = 1, kWhereProducerDep = 2, kWhereMmaFull = 3, kWhereMmaTmemEmpty = 4,
-    kWhereEpiTmemFull = 5, kWhereDispatch = 6, kWhereGemmOffsets = 7
+    kWhereEpiTmemFull = 5, kWhereDispatch = 6, kWhereGemmOffsets = 7, kWhereCombine = 8
 };
 
 // Default wall-clock limit of any single wait (ns). The longest legitimate

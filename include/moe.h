@@ -118,6 +118,11 @@ typedef struct {
                            the waits deadlock-free; interleaved schedule only (else
                            MOE_ERR_INVALID_ARG). The workspace must then come from
                            moe_workspace_bytes_tuned with the same tuning. */
+    int fused_combine;  /* moe_layer_forward_tuned / _ex only (else MOE_ERR_INVALID_ARG): 1 =
+                           combine inside the grouped GEMM (Cui et al. section 3.3: consumers
+                           poll the per-row Linear-2 completion and write each token to its
+                           owner segment as soon as its last expert row is finished); the
+                           output bits equal the separate combine's. 0 = separate kernel. */
 } moe_tuning_t;
 
 /* Human-readable name of a status code. Never NULL. */

@@ -160,3 +160,13 @@ def test_h_ring_workspace_layout_and_checks(lib):
     assert lib.moe_expert_ffn(c, fake, fake, fake, fake, fake, fake, fake, ring_nb, None) == \
         moe.MOE_ERR_WORKSPACE
 
+
+def test_fused_combine_belongs_to_the_layer_call(lib):
+    s = moe.Shape(T=64, d=64, E=4, top_k=2, ffn=64)
+    c = ctypes.byref(s.c())
+    fake = ctypes.c_void_p(1 << 20)
+    nb = moe.workspace_bytes(s)
+    for bad in (moe.Tuning(fused_combine=1), moe.Tuning(fused_combine=2)):
+        assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad.c()), fake, fake, fake, fake, fake, fake,
+                                        fake, nb, None) == moe.MOE_ERR_INVALID_ARG
+

@@ -117,6 +117,50 @@ def test_layer_with_h_ring_is_bit_identical():
     assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), a.view(torch.int16))
 
 
+FUSED_CASES = [custom_cfg(1000, 136, 5, 3, 200, S=8, zipf_s=2.0), custom_cfg(333, 256, 33, 4, 128, S=3, zipf_s=1.0),
+               custom_cfg(64, 512, 256, 8, 64), custom_cfg(1, 64, 4, 2, 64), custom_cfg(4096, 512, 8, 2, 256, S=4)]
+GEMM_MODES = {"m1": dict(cta_group=1, orientation=moe.ORIENT_TOKENS_M),
+              "m2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_M),
+              "n2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_N)}
+
+
+@pytest.mark.parametrize("mode", sorted(GEMM_MODES))
+@pytest.mark.parametrize("cfg", FUSED_CASES, ids=lambda c: f"T{c.T}_E{c.E}_S{c.S}")
+def test_fused_combine_is_bit_identical(cfg, mode):
+    """The combine done by consumer warps inside the grouped GEMM, each token
+    written once its last expert row is finished, gives the separate combine
+    kernel's bits (same fp32 sum in j order), into every owner segment."""
+    need_gpu()
+    layer = GpuLayer(cfg, seed=2)
+    a = layer.forward(tuning=moe.Tuning(**GEMM_MODES[mode])).clone()
+    for seg in layer.out:
+        seg.fill_(float("nan"))
+    b = layer.forward(tuning=moe.Tuning(**GEMM_MODES[mode], fused_combine=1))
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_fused_combine_with_h_ring_and_a_timeout():
+    """Fused combine over a ring-buffered h is still bit-identical; and when a
+    Linear-2 dependency can never be met the consumers give up with the rest
+    of the kernel (bounded waits) and the context stays usable."""
+    need_gpu()
+    cfg = custom_cfg(4096, 256, 8, 2, 256, S=2)
+    layer = GpuLayer(cfg, seed=3)
+    a = layer.forward().clone()
+    t = moe.Tuning(fused_combine=1, h_ring_rows=40)
+    ws = moe.alloc_workspace(layer.shape, tuning=t)
+    i = layer.inp
+    moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=t)
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), a.view(torch.int16))
+    bad = moe.Tuning(fused_combine=1, wait_limit_us=20000, unmet_dependency=1)
+    moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=bad)
+    assert moe.last_device_status(ws) == moe.MOE_ERR_TIMEOUT
+    moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=t)
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), a.view(torch.int16))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mid", "dit", "fine", "coarse"])
 def test_full_size_configs(name):
@@ -125,6 +169,8 @@ def test_full_size_configs(name):
     out = layer.forward()
     out2 = layer.forward(tuning=moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE))
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    out3 = layer.forward(tuning=moe.Tuning(fused_combine=1))
+    assert torch.equal(out.view(torch.int16), out3.view(torch.int16))
     maxrel, fro = _full_compare(layer, out, n_tokens=24, n_rows=48)
     print(f"{name}: max err / max|ref| = {maxrel:.2e}, rel Frobenius = {fro:.2e}")
     del layer
