@@ -38,8 +38,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// KMAX bounds k; each lane keeps U = 8 / KMAX column vectors of every expert
-// row in flight (16 loads of 16 bytes at most), so a small k still has enough
+// KMAX bounds k; each lane keeps U = 16 / KMAX column vectors of every expert
+// row in flight (up to 16 loads of 16 bytes), so few warps still have enough
 // memory-level parallelism to cover HBM latency.
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads)
@@ -47,7 +47,9 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ gate,
                const int32_t *__restrict__ row_of_slot, int T, int d, int k, int rows_per_seg,
                const Segments seg)
 {
-    constexpr int U = 8 / KMAX;
+    constexpr int U = 16 / KMAX;
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long t = static_cast<long>(blockIdx.x) * (kThreads / 32) + warp;
     if (t >= T) return;
@@ -95,12 +97,13 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s)
     for (int i = 0; i < kMaxSegments; ++i) seg.p[i] = i < a.S ? a.seg[i] : nullptr;
     const unsigned blocks = static_cast<unsigned>((a.T + kThreads / 32 - 1) / (kThreads / 32));
     if (a.k <= 2)
-        combine_kernel<2><<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S, seg);
-    else if (a.k <= 4)
-        combine_kernel<4><<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S, seg);
-    else
-        combine_kernel<8><<<blocks, kThreads, 0, s>>>(a.y, a.gate, a.row_of_slot, a.T, a.d, a.k, a.T / a.S, seg);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<2>, dim3(blocks), dim3(kThreads), 0, s, a.y, a.gate, a.row_of_slot,
+                          a.T, a.d, a.k, a.T / a.S, seg);
+    if (a.k <= 4)
+        return launch_pdl(combine_kernel<4>, dim3(blocks), dim3(kThreads), 0, s, a.y, a.gate, a.row_of_slot,
+                          a.T, a.d, a.k, a.T / a.S, seg);
+    return launch_pdl(combine_kernel<8>, dim3(blocks), dim3(kThreads), 0, s, a.y, a.gate, a.row_of_slot,
+                          a.T, a.d, a.k, a.T / a.S, seg);
 }
 
 }  // namespace moe

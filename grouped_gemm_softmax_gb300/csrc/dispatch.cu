@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restri
                                                          unsigned *status)
 {
     __shared__ int cnt[kMaxExperts];
+    pdl_wait();
+    pdl_trigger();
     for (int e = threadIdx.x; e < E; e += kThreads) cnt[e] = 0;
     __syncthreads();
     const long s0 = static_cast<long>(blockIdx.x) * C * k;
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t *chunk_base, int
     __shared__ int cells[kScanMaxCells];
     __shared__ int tot[kMaxExperts];
     __shared__ int warp_sums[kThreads / 32];
+    pdl_wait();
+    pdl_trigger();
     const int n = nchunks * E;
     for (int i = threadIdx.x; i < n; i += kThreads) cells[i] = chunk_base[i];
     __syncthreads();
@@ -103,6 +107,8 @@ __global__ void __launch_bounds__(kThreads) rank_kernel(const int32_t *__restric
     __shared__ int cur[kMaxExperts];            // running base per expert across batches
     __shared__ int wcnt[NW][kMaxExperts];       // per-warp counts, then per-warp bases
     __shared__ int sidx[kRankBatch];
+    pdl_wait();
+    pdl_trigger();
     for (int e = threadIdx.x; e < E; e += kThreads)
         cur[e] = chunk_base[static_cast<long>(blockIdx.x) * E + e];
     const long s0 = static_cast<long>(blockIdx.x) * C * k;
@@ -164,6 +170,8 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const uint16_t *__restri
                                                         const int32_t *__restrict__ row_of_slot,
                                                         int T, int d, int k, uint16_t *x_perm)
 {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long t = static_cast<long>(blockIdx.x) * (kThreads / 32) + warp;
     if (t >= T) return;
@@ -202,14 +210,19 @@ cudaError_t launch_dispatch(const DispatchArgs &a, cudaStream_t s)
     }
     const int C = a.chunk_tokens;
     const int nchunks = (a.T + C - 1) / C;
-    count_kernel<<<nchunks, kThreads, 0, s>>>(a.topk_idx, a.T, a.k, a.E, C, a.chunk_base, a.status);
-    scan_kernel<<<1, kThreads, 0, s>>>(a.chunk_base, nchunks, a.E, a.counts, a.offsets,
-                                       a.zero_words, a.zero_words ? a.zero_count : 0);
-    rank_kernel<<<nchunks, kThreads, 0, s>>>(a.topk_idx, a.T, a.k, a.E, C, a.chunk_base,
-                                             a.row_of_slot, a.slot_of_row);
+    cudaError_t err = launch_pdl(count_kernel, dim3(nchunks), dim3(kThreads), 0, s, a.topk_idx, a.T, a.k,
+                                 a.E, C, a.chunk_base, a.status);
+    if (err == cudaSuccess)
+        err = launch_pdl(scan_kernel, dim3(1), dim3(kThreads), 0, s, a.chunk_base, nchunks, a.E, a.counts,
+                         a.offsets, a.zero_words, a.zero_words ? a.zero_count : 0L);
+    if (err == cudaSuccess)
+        err = launch_pdl(rank_kernel, dim3(nchunks), dim3(kThreads), 0, s, a.topk_idx, a.T, a.k, a.E, C,
+                         static_cast<const int32_t *>(a.chunk_base), a.row_of_slot, a.slot_of_row);
     const unsigned copy_blocks = static_cast<unsigned>((a.T + kThreads / 32 - 1) / (kThreads / 32));
-    copy_kernel<<<copy_blocks, kThreads, 0, s>>>(a.x, a.row_of_slot, a.T, a.d, a.k, a.x_perm);
-    return cudaGetLastError();
+    if (err == cudaSuccess)
+        err = launch_pdl(copy_kernel, dim3(copy_blocks), dim3(kThreads), 0, s, a.x,
+                         static_cast<const int32_t *>(a.row_of_slot), a.T, a.d, a.k, a.x_perm);
+    return err;
 }
 
 }  // namespace moe

@@ -492,6 +492,10 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         tmem_relinquish<CG>();
         tc_fence_before();
     }
+    // everything above overlaps the previous kernel's tail; what follows reads
+    // its outputs (expert offsets, x_perm, counters)
+    pdl_wait();
+    pdl_trigger();
     if (warp == 2) {
         // expert offsets -> scheduler-row prefix (warp-parallel exclusive scan).
         // Offsets that are not a non-decreasing sequence from 0 to R are
@@ -1068,11 +1072,13 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(FC ? kThreads + kConsumerThreads : kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1128,6 +1134,7 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
         if (err != cudaSuccess) return err;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(instances * CG), 1, 1);
+    cfg.numAttrs = 2;  // + programmatic dependent launch (the occupancy query used the cluster alone)
     return cudaLaunchKernelEx(&cfg, grouped_swiglu_gemm_kernel<CG, TN, FC>, tx, th, tw1, tw3, tw2, p);
 }
 

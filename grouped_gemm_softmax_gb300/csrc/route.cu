@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(32 * WE * WT) route_kernel(const RouteParams p
     float *xs = rsm;            // [BT][LD]
     float *ws = rsm + BT * LD;  // [BE][LD]
     float *lg = rsm;            // [BT][BE + 1] (reused after the K loop)
+    pdl_wait();
+    pdl_trigger();
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -269,6 +271,8 @@ __global__ void __launch_bounds__(32 * WE * WT) route_kernel_async(const RoutePa
     constexpr int CPR = KB / 8;            // 16-byte copies per row
     extern __shared__ __align__(16) uint16_t rsm16[];
     float *lg = reinterpret_cast<float *>(rsm16);  // [BT][BE + 1] after the K loop
+    pdl_wait();
+    pdl_trigger();
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -371,8 +375,7 @@ cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
         attr = true;
     }
     const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
-    route_kernel<TM, TN, WE, WT, kBK><<<grid, NT, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(route_kernel<TM, TN, WE, WT, kBK>, dim3(grid), dim3(NT), smem, s, p);
 }
 
 template <int TM, int TN, int WE, int WT, int KB, int STAGES>
@@ -393,8 +396,7 @@ cudaError_t launch_variant_async(const RouteParams &p, cudaStream_t s)
         attr = true;
     }
     const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
-    route_kernel_async<TM, TN, WE, WT, KB, STAGES><<<grid, NT, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(route_kernel_async<TM, TN, WE, WT, KB, STAGES>, dim3(grid), dim3(NT), smem, s, p);
 }
 
 }  // namespace
