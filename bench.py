@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--h-ring", type=int, default=0,
                     help="h as a ring of this many scheduler rows (0 = every row in place)")
+    ap.add_argument("--row-order", default="default", choices=["default", "expert", "mixed"],
+                    help="order of the grouped GEMM's scheduler rows")
     ap.add_argument("--fused-combine", action="store_true",
                     help="combine inside the grouped GEMM (consumer warps) instead of a separate kernel")
     ap.add_argument("--timeline", action="store_true",
@@ -326,7 +328,8 @@ def run_ours(args, cfg):
               "tokens-n": moe.ORIENT_TOKENS_N}[args.orientation]
     tuning = moe.Tuning(schedule=moe.SCHEDULE_EXPERT_WAVE if args.schedule == "wave"
                         else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead, orientation=orient,
-                        h_ring_rows=args.h_ring, fused_combine=1 if args.fused_combine else 0)
+                        h_ring_rows=args.h_ring, fused_combine=1 if args.fused_combine else 0,
+                        row_order={"default": 0, "expert": 1, "mixed": 2}[args.row_order])
     ws = moe.alloc_workspace(shape, dev, tuning if args.h_ring else None)
     rows = cfg.T // cfg.S
     out = [torch.empty(rows, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
@@ -509,6 +512,8 @@ def run_ours(args, cfg):
         line["config"]["lead_rows"] = args.lead
     if args.orientation != "default":
         line["config"]["orientation"] = args.orientation
+    if args.row_order != "default":
+        line["config"]["row_order"] = args.row_order
     if args.fused_combine:
         line["config"]["fused_combine"] = True
         line["gpu_launches"] = (KERNELS_PER_STEP - 1) * args.steps

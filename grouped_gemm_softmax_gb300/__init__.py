@@ -57,7 +57,7 @@ class _CTuning(ctypes.Structure):
                 ("wait_limit_us", ctypes.c_int), ("unmet_dependency", ctypes.c_int),
                 ("trace", ctypes.c_void_p), ("tile_trace", ctypes.c_void_p),
                 ("tile_trace_cap", ctypes.c_int), ("orientation", ctypes.c_int),
-                ("h_ring_rows", ctypes.c_int), ("fused_combine", ctypes.c_int)]
+                ("h_ring_rows", ctypes.c_int), ("fused_combine", ctypes.c_int), ("row_order", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -102,13 +102,15 @@ class Tuning:
     orientation: int = ORIENT_DEFAULT  # which MMA operand holds the tokens (ORIENT_*)
     h_ring_rows: int = 0  # h as a ring of this many scheduler rows (0 = all rows)
     fused_combine: int = 0  # layer only: combine inside the grouped GEMM (consumer warps)
+    row_order: int = 0  # scheduler rows: 0 default, 1 expert order, 2 mixed (single-row experts spread out)
 
     def c(self) -> _CTuning:
         tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
         tt = None if self.tile_trace is None else _ptr(self.tile_trace, torch.int64, None, "tile_trace")
         return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
                         self.cta_group, self.wait_limit_us, self.unmet_dependency, tr, tt,
-                        self.tile_trace_cap, self.orientation, self.h_ring_rows, self.fused_combine)
+                        self.tile_trace_cap, self.orientation, self.h_ring_rows, self.fused_combine,
+                        self.row_order)
 
 
 _lib = None

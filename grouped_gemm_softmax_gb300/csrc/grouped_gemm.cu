@@ -99,6 +99,8 @@ constexpr int kTraceWords = 16;  // per-CTA counters when tracing is on
 // issue, 5 MMA stage-wait cycles, 6 epilogue start (accumulator ready),
 // 7 epilogue stores done
 constexpr int kTileTraceWords = 8;
+constexpr int kMaxMixedRows = 1024;  // scheduler rows the mixed order can hold
+constexpr bool kMixedByDefault = true;
 
 template <int CG>
 struct Cfg {
@@ -120,6 +122,7 @@ struct GemmParams {
     int kb1, kb2;
     int schedule, lead, group, cg;
     int ring;  // h ring slots in scheduler rows; 0 = h holds every row
+    int mixed; // mixed row order: 0 off, 1 when single-row experts are >= 1/4 of the rows, 2 asked for
     int fc;    // fused combine: count finished Linear-2 tiles per row for the consumers
     const float *gate;
     const int32_t *row_of_slot;
@@ -150,6 +153,8 @@ struct SmemCtl {
     int row_start[kMaxExperts + 1];  // first scheduler row of each expert
     int wave_row[kMaxExperts + 1];   // wave w spans scheduler rows [wave_row[w], wave_row[w+1])
     int wave_tile[kMaxExperts + 1];  // first global tile index of wave w
+    int mixed;                       // scheduler rows in the mixed order (mrow) instead of expert order
+    int mrow[kMaxMixedRows];         // mixed order: scheduler row -> expert | band << 9
 };
 
 // epilogue buffer per epilogue warp: tokens on the M side use 32 rows x 64
@@ -168,6 +173,7 @@ struct Tile {
     int row;   // scheduler row
     int n;     // N-tile
     int e;     // expert owning the row
+    int b0;    // the row's first token row (in x_perm / y_perm)
 };
 
 // Position k of a tile stream (Pn N-tiles per scheduler row) -> (row, n). Tiles
@@ -180,20 +186,34 @@ struct Tile {
 struct StreamCursor {
     int e = 0;
 
-    __device__ Tile at(const SmemCtl &c, int E, int k, int Pn, int GM, int kind)
+    __device__ Tile at(const SmemCtl &c, int E, int k, int Pn, int GM, int kind, int rows)
     {
-        while (e + 1 < E && c.row_start[e + 1] * Pn <= k) ++e;
         Tile t;
         t.kind = kind;
+        const int per_group = GM * Pn;
+        if (c.mixed) {
+            // mixed order: the raster groups run over the global row sequence
+            const int P = c.row_start[E];
+            const int j = k / per_group;
+            const int gs = min(GM, P - j * GM);
+            const int i = k - j * per_group;
+            t.n = i / gs;
+            t.row = j * GM + i % gs;
+            const int packed = c.mrow[t.row];
+            t.e = packed & 0x1FF;
+            t.b0 = c.offs[t.e] + (packed >> 9) * rows;
+            return t;
+        }
+        while (e + 1 < E && c.row_start[e + 1] * Pn <= k) ++e;
         t.e = e;
         const int r0 = c.row_start[e];
         const int local = k - r0 * Pn;
-        const int per_group = GM * Pn;
         const int j = local / per_group;
         const int gs = min(GM, c.row_start[e + 1] - r0 - j * GM);
         const int i = local - j * per_group;
         t.n = i / gs;
         t.row = r0 + j * GM + i % gs;
+        t.b0 = c.offs[e] + (t.row - r0) * rows;
         return t;
     }
 };
@@ -204,7 +224,7 @@ struct Scheduler {
     int k1, k2, tot1, tot2;
     int gi;
     int w;
-    int P1, P2, G, D, GM, mode;
+    int P1, P2, G, D, GM, mode, rows;
     StreamCursor s1, s2;
     Tile t2;         // decoded Linear-2 tile at k2 (interleaved mode)
     bool t2_valid;
@@ -218,6 +238,7 @@ struct Scheduler {
         D = p.lead;
         GM = p.group;
         mode = p.schedule;
+        rows = p.cg * kBlockM;  // token rows of one scheduler row
         k1 = k2 = blockIdx.x / p.cg;
         tot1 = P * P1;
         tot2 = P * P2;
@@ -239,7 +260,7 @@ struct Scheduler {
             const int p1 = (k1 < tot1) ? k1 / P1 : INT_MAX / 2;
             if (k2 < tot2) {
                 if (!t2_valid) {
-                    t2 = s2.at(c, E, k2, P2, GM, 1);
+                    t2 = s2.at(c, E, k2, P2, GM, 1, rows);
                     t2_valid = true;
                 }
                 if (t2.row + D <= p1) {
@@ -248,7 +269,7 @@ struct Scheduler {
                     return t2;
                 }
             }
-            t = s1.at(c, E, k1, P1, GM, 0);
+            t = s1.at(c, E, k1, P1, GM, 0, rows);
             k1 += G;
             return t;
         }
@@ -262,8 +283,8 @@ struct Scheduler {
         const int r0 = c.wave_row[w];
         const int nr = c.wave_row[w + 1] - r0;
         gi += G;
-        if (j < nr * P1) return s1.at(c, E, r0 * P1 + j, P1, GM, 0);
-        return s2.at(c, E, r0 * P2 + (j - nr * P1), P2, GM, 1);
+        if (j < nr * P1) return s1.at(c, E, r0 * P1 + j, P1, GM, 0, rows);
+        return s2.at(c, E, r0 * P2 + (j - nr * P1), P2, GM, 1, rows);
     }
 };
 
@@ -535,6 +556,62 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
         if (lane == 31) c.row_start[E] = incl;
         __syncwarp();
+        // Mixed row order: experts with a single scheduler row ("light": their
+        // tiles mostly stream weights) are spread evenly among the rows of the
+        // other experts ("heavy": their tiles are compute-bound), so that the
+        // tiles in flight at any time mix both. Light row i goes to position
+        // ceil((i+1)P/l) - 1, heavy row j to the (j+1)-th remaining position
+        // (Bresenham over P = h + l rows); positions of one raster group share
+        // an N-tile, so the heavy rows still reuse their weight tiles.
+        int mixed = 0;
+        if (p.mixed && !any_bad) {
+            int lc = 0, hc = 0;
+            for (int i = 0; i < per; ++i) {
+                const int e = lane * per + i;
+                if (e < E) {
+                    const int nb = c.row_start[e + 1] - c.row_start[e];
+                    if (nb == 1) ++lc;
+                    else hc += nb;
+                }
+            }
+            int li = lc, hi = hc;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, li, o);
+                const int b = __shfl_up_sync(0xffffffffu, hi, o);
+                if (lane >= o) {
+                    li += a;
+                    hi += b;
+                }
+            }
+            const int l = __shfl_sync(0xffffffffu, li, 31), h = __shfl_sync(0xffffffffu, hi, 31);
+            const int P = l + h;
+            li -= lc;  // this lane's first light index / heavy row index
+            hi -= hc;
+            // worth it when single-row experts make up a quarter of the rows or
+            // more (mid: 34%, -2.5% GEMM time); with few of them, groups that
+            // straddle two large experts lose weight reuse (DiT: +2.7%)
+            if (l > 0 && h > 0 && P <= kMaxMixedRows && (p.mixed == 2 || 4 * l >= P)) {
+                mixed = 1;
+                for (int i = 0; i < per; ++i) {
+                    const int e = lane * per + i;
+                    if (e >= E) break;
+                    const int nb = c.row_start[e + 1] - c.row_start[e];
+                    if (nb == 1) {
+                        c.mrow[((li + 1) * P + l - 1) / l - 1] = e;
+                        ++li;
+                    } else {
+                        for (int bnd = 0; bnd < nb; ++bnd, ++hi) {
+                            // smallest x with x - floor(x l / P) >= hi + 1; the row sits at x - 1
+                            int x = hi * P / h + 1;
+                            while (x - x * l / P < hi + 1) ++x;
+                            c.mrow[x - 1] = e | (bnd << 9);
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0) c.mixed = mixed;
+        __syncwarp();
         if (lane == 0) {
             // expert waves for the comparison schedule: consecutive experts until
             // the wave's Linear-1 tiles fill the grid once
@@ -580,7 +657,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         : nullptr;
                 unsigned long long dep0 = rec ? clock64() : 0;
                 const int e = t.e;
-                const int band0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows;
+                const int band0 = t.b0;
                 // this CTA's 128 rows of the scheduler row (tokens on the M side)
                 const int row0 = band0 + static_cast<int>(rank) * kBlockM;
                 // this CTA's first token of B (tokens on the N side)
@@ -705,7 +782,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b) * kAccCols;
                 uint32_t idesc = t.kind == 0 ? idesc1 : idesc2;
                 if constexpr (TN) {
-                    const int band0 = c.offs[t.e] + (t.row - c.row_start[t.e]) * kTileRows;
+                    const int band0 = t.b0;
                     idesc = idesc_bf16_f32(kTileRows, tile_tokens(c.offs[t.e + 1] - band0, kTileRows));
                 }
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
@@ -798,8 +875,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             }
             tc_fence_after();
             const int e = t.e;
-            const int row0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows +
-                             static_cast<int>(rank) * kBlockM;
+            const int row0 = t.b0 + static_cast<int>(rank) * kBlockM;
             if constexpr (TN) {
                 // accumulator: lane = weight row, column = token. Per 32-token
                 // slab each warp works alone: Linear-1 lanes l and l+16 hold
@@ -807,7 +883,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 // 0-15 and lane l+16 tokens 16-31 of that feature; the bf16
                 // results go token-major into the warp's shared-memory slab,
                 // and lane j stores token j's contiguous columns.
-                const int band0 = c.offs[e] + (t.row - c.row_start[e]) * kTileRows;
+                const int band0 = t.b0;
                 const int valid = min(kTileRows, c.offs[e + 1] - band0);
                 uint8_t *wslab = s_epi + (warp - 2) * kEpiStageBytes;
                 const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -900,8 +976,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 const int nchunks = t.kind == 0 ? kL1N / 64 : p.N2 / 64;
                 // h rows go to the row's ring slot when the ring is on
                 const long hoff = (t.kind == 0 && p.ring)
-                                      ? static_cast<long>(t.row % p.ring) * kTileRows -
-                                            (c.offs[e] + (t.row - c.row_start[e]) * kTileRows)
+                                      ? static_cast<long>(t.row % p.ring) * kTileRows - t.b0
                                       : 0;
                 uint16_t *const out_base = t.kind == 0 ? p.h + hoff * p.F : p.y;
                 const int out_ld = t.kind == 0 ? p.F : p.d;
@@ -1150,6 +1225,13 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.l1_done = a.l1_done;
     p.l2_done = a.l1_done + a.max_rows;
     p.ring = a.h_ring_rows;
+    // mixed row order: asked for (or by default) with the interleaved schedule;
+    // not with the fused combine, whose consumers walk rows in expert order
+    // 2 = asked for: taken whenever both kinds of experts exist; 1 = default:
+    // taken when single-row experts are a quarter of the rows or more
+    p.mixed = (a.schedule == 0 && a.gate == nullptr)
+                  ? (a.row_order == 2 ? 2 : (a.row_order == 0 && kMixedByDefault) ? 1 : 0)
+                  : 0;
     p.l2_flags = a.l2_flags;
     p.status = a.status;
     p.E = a.E;

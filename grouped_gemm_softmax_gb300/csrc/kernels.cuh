@@ -83,6 +83,7 @@ struct FfnArgs {
     int schedule, lead, num_ctas, l2_block_n, group_rows, cta_group;
     int orientation;  // 0 = choose, 1 = tokens on the MMA's M side, 2 = on its N side
     int h_ring_rows;  // h ring slots in scheduler rows (0 = h holds every row)
+    int row_order;    // 0 = default, 1 = expert order, 2 = mixed (single-row experts spread out)
     // fused combine (consumer warps in the GEMM kernel); gate == nullptr = off
     const float *gate;            // [T,k]
     const int32_t *row_of_slot;   // [R]

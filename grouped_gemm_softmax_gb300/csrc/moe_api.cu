@@ -146,6 +146,7 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->h_ring_rows < 0 || (t->h_ring_rows > 0 && t->schedule != MOE_SCHEDULE_INTERLEAVED))
         return MOE_ERR_INVALID_ARG;
     if (t->fused_combine < 0 || t->fused_combine > 1) return MOE_ERR_INVALID_ARG;
+    if (t->row_order < 0 || t->row_order > 2) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -188,6 +189,7 @@ moe_status_t enqueue_ffn(const moe_shape_t *s, const moe_tuning_t *tune, const L
     a.cta_group = tune ? tune->cta_group : 0;
     a.orientation = tune ? tune->orientation : 0;
     a.h_ring_rows = tune ? tune->h_ring_rows : 0;
+    a.row_order = tune ? tune->row_order : 0;
     a.wait_limit_us = tune ? tune->wait_limit_us : 0;
     a.unmet_dependency = tune ? tune->unmet_dependency : 0;
     a.trace = tune ? static_cast<unsigned long long *>(tune->trace) : nullptr;

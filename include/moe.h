@@ -123,6 +123,13 @@ typedef struct {
                            poll the per-row Linear-2 completion and write each token to its
                            owner segment as soon as its last expert row is finished); the
                            output bits equal the separate combine's. 0 = separate kernel. */
+    int row_order;      /* order of the scheduler rows: 1 = expert order, 2 = mixed (experts with
+                           a single row spread evenly among the other experts' rows, so
+                           weight-streaming and compute-bound tiles run side by side; taken with
+                           the interleaved schedule when both kinds exist and the rows number at
+                           most 1024, never with fused_combine), 0 = default (mixed when
+                           single-row experts are at least a quarter of the rows, else expert
+                           order). Results are bit-identical either way. */
 } moe_tuning_t;
 
 /* Human-readable name of a status code. Never NULL. */

@@ -170,3 +170,13 @@ def test_fused_combine_belongs_to_the_layer_call(lib):
         assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad.c()), fake, fake, fake, fake, fake, fake,
                                         fake, nb, None) == moe.MOE_ERR_INVALID_ARG
 
+
+def test_row_order_values_are_checked(lib):
+    s = moe.Shape(T=64, d=64, E=4, top_k=2, ffn=64)
+    c = ctypes.byref(s.c())
+    fake = ctypes.c_void_p(1 << 20)
+    nb = moe.workspace_bytes(s)
+    for bad in (moe.Tuning(row_order=3), moe.Tuning(row_order=-1)):
+        assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad.c()), fake, fake, fake, fake, fake, fake,
+                                        fake, nb, None) == moe.MOE_ERR_INVALID_ARG
+

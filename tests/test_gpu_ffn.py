@@ -91,7 +91,9 @@ def test_ffn_schedules_and_grids_are_bit_identical(mode):
     _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(**MODES[mode]))
     variants = [dict(schedule=moe.SCHEDULE_EXPERT_WAVE), dict(lead_rows=1), dict(lead_rows=50),
                 dict(num_ctas=2), dict(num_ctas=7), dict(group_rows=1), dict(group_rows=4),
-                dict(schedule=moe.SCHEDULE_EXPERT_WAVE, num_ctas=6, group_rows=2)]
+                dict(schedule=moe.SCHEDULE_EXPERT_WAVE, num_ctas=6, group_rows=2),
+                dict(row_order=1), dict(row_order=2), dict(row_order=2, num_ctas=6, group_rows=2),
+                dict(row_order=2, lead_rows=1)]
     for v in variants:
         t = moe.Tuning(**MODES[mode], **v)
         _, _, h, y = run_ffn(c, tuning=t)
@@ -149,8 +151,8 @@ def test_h_ring_is_bit_identical_to_full_h(mode):
     base = dict(MODES[mode], group_rows=4)
     _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(**base))
     group = 4 // MODES[mode]["cta_group"]  # raster group in scheduler rows
-    for ring in (2 * group + 1, 12):
-        t = moe.Tuning(**base, h_ring_rows=ring)
+    for ring, order in ((2 * group + 1, 0), (12, 0), (2 * group + 1, 2)):
+        t = moe.Tuning(**base, h_ring_rows=ring, row_order=order)
         s = moe.Shape(T=c["R"], d=c["d"], E=c["E"], top_k=1, ffn=c["F"])
         ws = moe.alloc_workspace(s, tuning=t)
         assert ws.numel() < moe.workspace_bytes(s)

@@ -171,6 +171,9 @@ def test_full_size_configs(name):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     out3 = layer.forward(tuning=moe.Tuning(fused_combine=1))
     assert torch.equal(out.view(torch.int16), out3.view(torch.int16))
+    for order in (1, 2):
+        out4 = layer.forward(tuning=moe.Tuning(row_order=order))
+        assert torch.equal(out.view(torch.int16), out4.view(torch.int16))
     maxrel, fro = _full_compare(layer, out, n_tokens=24, n_rows=48)
     print(f"{name}: max err / max|ref| = {maxrel:.2e}, rel Frobenius = {fro:.2e}")
     del layer
