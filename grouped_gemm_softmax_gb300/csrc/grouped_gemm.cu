@@ -4,9 +4,12 @@
 // Computation-Communication Overlap ...", section 3.3.1: one rank-wide
 // persistent kernel over a unified tile worklist with per-tile ready flags).
 //
-// Tiles. Rows of x_perm are expert-contiguous. A "scheduler row" is one
-// 128-row M-tile of one expert; the scheduler rows of all experts are
-// concatenated in expert order (row p -> expert e(p), first row O_e).
+// Tiles. Rows of x_perm are expert-contiguous. A "scheduler row" is one band
+// of 128 (single CTA) or 256 (CTA pair) token rows of one expert; the
+// scheduler rows of all experts are concatenated in expert order (row p ->
+// expert e(p), first row O_e), or, in the mixed order, the rows of experts
+// that have a single row are spread evenly among the others' (see the
+// prologue).
 //   Linear-1 tile (p, n): h[rows, n*128 : n*128+128] =
 //       bf16(silu(x W1[e]^T) * (x W3[e]^T)); the MMA is 128 x 256 x 16 with the
 //       W1 tile stacked on the W3 tile, so one accumulator holds gate | up.
@@ -45,10 +48,11 @@
 // (all Linear-1 tiles of a wave of experts, then its Linear-2 tiles) is kept
 // as the comparison schedule. Both orders give bit-identical outputs.
 //
-// CTA roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
-// allocator + single-thread MMA issuer, warps 2..5 = epilogue (warp w reads
-// tensor-memory lanes 32*(w%4)...+31). Tensor memory holds two 128 x 256 fp32
-// accumulators (512 columns).
+// CTA roles (192 threads, 256 with the fused combine): warp 0 = TMA producer,
+// warp 1 = tensor-memory allocator + single-thread MMA issuer, warps 2..5 =
+// epilogue (warp w reads tensor-memory lanes 32*(w%4)...+31), warps 6..7 =
+// combine consumers. Tensor memory holds two 128 x 256 fp32 accumulators (512
+// columns).
 //
 // CTA pairs (CG = 2, the default): the two CTAs of a cluster compute 256-row
 // tiles with tcgen05.mma.cta_group::2. Each CTA loads its own 128 rows of A and
