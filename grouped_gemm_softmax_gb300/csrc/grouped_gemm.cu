@@ -106,11 +106,13 @@ constexpr int kTileTraceWords = 8;
 constexpr int kMaxMixedRows = 1024;  // scheduler rows the mixed order can hold
 constexpr bool kMixedByDefault = true;
 
-template <int CG>
+template <int CG, bool TN = false>
 struct Cfg {
     static constexpr int kStages = CG == 2 ? 6 : 4;
     static constexpr int kBTileBytes = (256 / CG) * kBlockK * 2;  // this CTA's share of B
-    static constexpr int kTileRows = kBlockM * CG;                // rows of one scheduler row
+    // token rows of one scheduler row: the MMA's M rows with tokens on the M
+    // side; up to 256 tokens (the widest MMA N) with tokens on the N side
+    static constexpr int kTileRows = TN ? 256 : kBlockM * CG;
 };
 
 struct GemmParams {
@@ -127,6 +129,7 @@ struct GemmParams {
     int schedule, lead, group, cg;
     int ring;  // h ring slots in scheduler rows; 0 = h holds every row
     int mixed; // mixed row order: 0 off, 1 when single-row experts are >= 1/4 of the rows, 2 asked for
+    int rows;  // token rows of one scheduler row
     int fc;    // fused combine: count finished Linear-2 tiles per row for the consumers
     const float *gate;
     const int32_t *row_of_slot;
@@ -242,7 +245,7 @@ struct Scheduler {
         D = p.lead;
         GM = p.group;
         mode = p.schedule;
-        rows = p.cg * kBlockM;  // token rows of one scheduler row
+        rows = p.rows;  // token rows of one scheduler row
         k1 = k2 = blockIdx.x / p.cg;
         tot1 = P * P1;
         tot2 = P * P2;
@@ -358,10 +361,10 @@ __device__ __forceinline__ int last_le(const int *v, int n, int x)
 // over many CTAs), wait until the unit's row has all its Linear-2 tiles
 // finished, and combine every token whose last row lies in the unit. False
 // when a wait gave up.
-template <int CG>
+template <int CG, bool TN>
 __device__ bool combine_consumer(SmemCtl &c, const GemmParams &p, int lane, volatile int *abort_flag)
 {
-    constexpr int kTileRows = Cfg<CG>::kTileRows;
+    constexpr int kTileRows = Cfg<CG, TN>::kTileRows;
     constexpr int kUnits = kTileRows / 32;
     const int E = p.E;
     const int P = c.row_start[E];
@@ -477,7 +480,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     uint8_t *sA = reinterpret_cast<uint8_t *>(base);
     constexpr int kStages = Cfg<CG>::kStages;
     constexpr int kBTileBytes = Cfg<CG>::kBTileBytes;
-    constexpr int kTileRows = Cfg<CG>::kTileRows;
+    constexpr int kTileRows = Cfg<CG, TN>::kTileRows;
     uint8_t *sB = sA + kStages * kATileBytes;
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(sB + kStages * kBTileBytes);
     uint8_t *s_epi = sB + kStages * kBTileBytes + kCtlBytes;
@@ -487,7 +490,9 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int E = p.E;
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // CTA within the pair
     const bool leader = rank == 0;
-    static_assert(!TN || CG == 2, "tokens on the N side needs CTA pairs");
+    // tokens on the N side: weight rows (features) a tile covers in this CTA:
+    // Linear-1 64 (64 W1 over the same 64 W3 rows), Linear-2 128 W2 rows
+    constexpr int kTnL1 = 64, kTnL2 = kBlockM;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -719,13 +724,13 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                     if constexpr (TN) {
                         if (t.kind == 0) {
                             // 64 W1 rows over the same 64 W3 rows, then the tokens
-                            const int f = t.n * kL1N + static_cast<int>(rank) * (kL1N / 2);
+                            const int f = t.n * (kTnL1 * CG) + static_cast<int>(rank) * kTnL1;
                             tma_load_3d<CG>(&tm_w1, bar, a, kb * kBlockK, f, e);
                             tma_load_3d<CG>(&tm_w3, bar, a + kATileBytes / 2, kb * kBlockK, f, e);
                             tma_load_2d<CG>(&tm_x, bar, b, kb * kBlockK, brow);
                         } else {
                             tma_load_3d<CG>(&tm_w2, bar, a, kb * kBlockK,
-                                            t.n * p.N2 + static_cast<int>(rank) * kBlockM, e);
+                                            t.n * p.N2 + static_cast<int>(rank) * kTnL2, e);
                             tma_load_2d<CG>(&tm_h, bar, b, kb * kBlockK, brow + hoff);
                         }
                     } else if (t.kind == 0) {
@@ -787,7 +792,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 uint32_t idesc = t.kind == 0 ? idesc1 : idesc2;
                 if constexpr (TN) {
                     const int band0 = t.b0;
-                    idesc = idesc_bf16_f32(kTileRows, tile_tokens(c.offs[t.e + 1] - band0, kTileRows));
+                    idesc = idesc_bf16_f32(kBlockM * CG, tile_tokens(c.offs[t.e + 1] - band0, kTileRows));
                 }
                 const int nkb = t.kind == 0 ? p.kb1 : p.kb2;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -837,7 +842,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
     } else if (FC && warp >= kThreads / 32) {
         // ------------------------------------------------------------ combine consumers
-        combine_consumer<CG>(c, p, lane, abort_flag);
+        combine_consumer<CG, TN>(c, p, lane, abort_flag);
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
@@ -934,7 +939,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         // two lanes a token, 32 bytes each
                         const int tk = (gate_w ? 0 : 16) + (lane >> 1);
                         const int half = lane & 1;
-                        const int col = t.n * kL1N + static_cast<int>(rank) * (kL1N / 2) + (q & 1) * 32 +
+                        const int col = t.n * (kTnL1 * CG) + static_cast<int>(rank) * kTnL1 + (q & 1) * 32 +
                                         half * 16;
                         const long hrow = static_cast<long>(band0) + ch * 32 + tk +
                                           (p.ring ? (t.row % p.ring) * kTileRows - band0 : 0);
@@ -958,7 +963,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                             sl[(2 * i + (ev ? 0 : 1)) * 16 + (lane >> 1)] = pack_bf16x2(lo_v, hi_v);
                         }
                         __syncwarp();
-                        const int col = t.n * p.N2 + static_cast<int>(rank) * kBlockM + q * 32;
+                        const int col = t.n * p.N2 + static_cast<int>(rank) * kTnL2 + q * 32;
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
                             const int j = (jj + (lane >> 1)) & 3;  // spread the lanes over the banks
@@ -1059,7 +1064,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         // with the fused combine, the epilogue warps turn consumers once their
         // tiles are done (unless a wait gave up)
         if constexpr (FC)
-            if (!*abort_flag && ld_volatile_u32(p.status) == 0u) combine_consumer<CG>(c, p, lane, abort_flag);
+            if (!*abort_flag && ld_volatile_u32(p.status) == 0u)
+                combine_consumer<CG, TN>(c, p, lane, abort_flag);
         if (tr && publisher) {
             unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
             o[6] = w_full;
@@ -1199,9 +1205,12 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
 
     const long R = a.R;
     CUtensorMap tx, th, tw1, tw3, tw2;
-    if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, kBlockM) ||
-        !make_map_2d(&th, a.h, a.F, p.ring ? static_cast<long>(p.ring) * Cfg<CG>::kTileRows : R, kBlockK,
-                     kBlockM) ||
+    // token boxes: the A rows with tokens on the M side, this CTA's B rows (all
+    // of a single CTA's up to 256 tokens, half of a pair's) on the N side
+    const uint32_t tok_box = TN ? 256 / CG : kBlockM;
+    if (!make_map_2d(&tx, a.x_perm, a.d, R, kBlockK, tok_box) ||
+        !make_map_2d(&th, a.h, a.F, p.ring ? static_cast<long>(p.ring) * Cfg<CG, TN>::kTileRows : R, kBlockK,
+                     tok_box) ||
         !make_map_3d(&tw1, a.w1, a.d, a.F, a.E, kBlockK, TN ? kL1N / 2 : kL1N) ||
         !make_map_3d(&tw3, a.w3, a.d, a.F, a.E, kBlockK, TN ? kL1N / 2 : kL1N) ||
         !make_map_3d(&tw2, a.w2, a.F, a.d, a.E, kBlockK, TN ? kBlockM : p.N2 / CG))
@@ -1244,9 +1253,9 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.R = a.R;
     // CTA pairs halve the operand traffic per MMA. With tokens on the M side
     // they pad every expert to 256-row tiles, so below ~1024 rows per expert
-    // single CTAs win there; with tokens on the N side (pairs only) an expert
-    // pads to 16 tokens. Tokens go on the N side unless Linear-2's 256-wide
-    // weight tiles would pad y (d not a multiple of 256) on large experts.
+    // single CTAs win there; with tokens on the N side an expert pads to 16
+    // tokens. Tokens go on the N side unless Linear-2's 256-wide weight tiles
+    // would pad y (d not a multiple of 256) on large experts.
     const bool big_experts = a.R / a.E >= 1024;
     bool tn;
     if (a.orientation == 2)
@@ -1256,13 +1265,15 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     else
         tn = a.d % 256 == 0 || !big_experts;
     if (tn)
-        p.cg = 2;
+        p.cg = a.cta_group == 1 ? 1 : 2;
     else if (a.cta_group == 1 || a.cta_group == 2)
         p.cg = a.cta_group;
     else
         p.cg = big_experts ? 2 : 1;
-    p.N2 = tn ? 2 * kBlockM : ffn_l2_block_n(a.d, a.l2_block_n);
-    p.P1 = (a.F + kL1N - 1) / kL1N;
+    p.rows = tn ? 256 : p.cg * kBlockM;
+    p.N2 = tn ? p.cg * kBlockM : ffn_l2_block_n(a.d, a.l2_block_n);
+    const int l1n = tn ? 64 * p.cg : kL1N;  // h columns per Linear-1 tile
+    p.P1 = (a.F + l1n - 1) / l1n;
     p.P2 = (a.d + p.N2 - 1) / p.N2;
     p.kb1 = (a.d + kBlockK - 1) / kBlockK;
     p.kb2 = (a.F + kBlockK - 1) / kBlockK;
@@ -1285,11 +1296,11 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
         p.k = a.k;
         p.rows_per_seg = a.T / a.S;
         for (int i = 0; i < kMaxSegments; ++i) p.seg[i] = i < a.S ? a.seg[i] : nullptr;
-        if (tn) return launch_cg<2, true, true>(a, p, stream);
+        if (tn) return p.cg == 1 ? launch_cg<1, true, true>(a, p, stream) : launch_cg<2, true, true>(a, p, stream);
         if (p.cg == 1) return launch_cg<1, false, true>(a, p, stream);
         return launch_cg<2, false, true>(a, p, stream);
     }
-    if (tn) return launch_cg<2, true, false>(a, p, stream);
+    if (tn) return p.cg == 1 ? launch_cg<1, true, false>(a, p, stream) : launch_cg<2, true, false>(a, p, stream);
     if (p.cg == 1) return launch_cg<1, false, false>(a, p, stream);
     return launch_cg<2, false, false>(a, p, stream);
 }

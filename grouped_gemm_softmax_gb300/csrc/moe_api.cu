@@ -141,7 +141,6 @@ moe_status_t check_tuning(const moe_tuning_t *t)
     if (t->tile_trace && (t->tile_trace_cap <= 0 || (reinterpret_cast<uintptr_t>(t->tile_trace) & 7u)))
         return MOE_ERR_INVALID_ARG;
     if (t->orientation < 0 || t->orientation > 2) return MOE_ERR_INVALID_ARG;
-    if (t->orientation == 2 && t->cta_group == 1) return MOE_ERR_INVALID_ARG;
     if (t->trace && (reinterpret_cast<uintptr_t>(t->trace) & 7u)) return MOE_ERR_INVALID_ARG;
     if (t->h_ring_rows < 0 || (t->h_ring_rows > 0 && t->schedule != MOE_SCHEDULE_INTERLEAVED))
         return MOE_ERR_INVALID_ARG;

@@ -72,16 +72,17 @@ typedef enum {
 
 /* Operand orientation of the grouped GEMM. Tokens on the M side: each MMA tile
    is 128 (single CTA) or 256 (CTA pair) token rows by a block of weight rows,
-   and every expert's last tile is padded to that height. Tokens on the N side
-   (CTA pairs only): each tile is 256 weight rows by up to 256 tokens, the
-   width rounded up to 16 tokens, so an expert pads at most 15 tokens. The
+   and every expert's last tile is padded to that height. Tokens on the N side:
+   each tile is 128 (single CTA) or 256 (CTA pair) weight rows by up to 256
+   tokens, the width rounded up to 16 tokens, so an expert pads at most 15
+   tokens. The
    default puts tokens on the N side unless d is not a multiple of 256 and the
    experts average 1024 rows or more. Results agree within the rounding of the
    fp32 accumulation order. */
 typedef enum {
     MOE_ORIENT_DEFAULT = 0,
     MOE_ORIENT_TOKENS_M = 1,
-    MOE_ORIENT_TOKENS_N = 2 /* with cta_group 0 or 2 (else MOE_ERR_INVALID_ARG) */
+    MOE_ORIENT_TOKENS_N = 2
 } moe_orientation_t;
 
 typedef struct {
@@ -95,8 +96,8 @@ typedef struct {
     int group_rows; /* raster group: an expert's tiles run N-tile-major over groups of this many
                        128-row M-tiles, so each weight tile is reused while hot in L2; 0 = default */
     int cta_group;  /* CTAs per MMA tile: 2 = CTA pairs with 256-row tiles, 1 = single CTAs
-                       with 128-row tiles (tokens on the M side only); 0 = default (pairs, except
-                       tokens on the M side with T*k/E < 1024) */
+                       with 128-row (tokens on M) or 128-weight-row (tokens on N) tiles;
+                       0 = default (pairs, except tokens on the M side with T*k/E < 1024) */
     int wait_limit_us;    /* limit of every bounded wait in the grouped GEMM; 0 = 2 s */
     int unmet_dependency; /* failure-detection test only: 1 makes each Linear-2 tile wait for one
                              more finished Linear-1 tile than exists, so the wait runs out and the

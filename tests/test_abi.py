@@ -101,8 +101,8 @@ def test_null_pointers_and_small_workspace_are_rejected_on_the_host(lib):
     bad_tune = moe.Tuning(schedule=7)
     assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad_tune.c()), fake, fake, fake, fake, fake, fake,
                                     fake, nb, None) == moe.MOE_ERR_INVALID_ARG
-    for bad in (dict(orientation=moe.ORIENT_TOKENS_N, cta_group=1), dict(orientation=3)):
-        bad_tune = moe.Tuning(**bad)  # tokens as N columns needs CTA pairs; 3 is no orientation
+    for bad in (dict(orientation=3), dict(orientation=-1)):
+        bad_tune = moe.Tuning(**bad)  # no such orientation
         assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad_tune.c()), fake, fake, fake, fake, fake, fake,
                                         fake, nb, None) == moe.MOE_ERR_INVALID_ARG
     bad_tune = moe.Tuning(l2_block_n=48)

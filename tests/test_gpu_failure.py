@@ -34,10 +34,10 @@ def _case(counts, d, F):
 
 
 MODES = [dict(cta_group=1, orientation=moe.ORIENT_TOKENS_M), dict(cta_group=2, orientation=moe.ORIENT_TOKENS_M),
-         dict(cta_group=2, orientation=moe.ORIENT_TOKENS_N)]
+         dict(cta_group=1, orientation=moe.ORIENT_TOKENS_N), dict(cta_group=2, orientation=moe.ORIENT_TOKENS_N)]
 
 
-@pytest.mark.parametrize("mode", MODES, ids=["m1", "m2", "n2"])
+@pytest.mark.parametrize("mode", MODES, ids=["m1", "m2", "n1", "n2"])
 def test_unmet_dependency_times_out_and_the_context_survives(mode):
     need_gpu()
     counts, off, x, w1, w3, w2 = _case([300, 40, 0, 513], 256, 384)

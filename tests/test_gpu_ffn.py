@@ -65,11 +65,14 @@ CASES = {
 # rows, pairs with tokens as N columns
 MODES = {"m1": dict(cta_group=1, orientation=moe.ORIENT_TOKENS_M),
          "m2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_M),
+         "n1": dict(cta_group=1, orientation=moe.ORIENT_TOKENS_N),
          "n2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_N)}
-TILE_ROWS = {"m1": 128, "m2": 256, "n2": 256}
+TILE_ROWS = {"m1": 128, "m2": 256, "n1": 256, "n2": 256}  # token rows of a scheduler row
+L1_COLS = {"m1": 128, "m2": 128, "n1": 64, "n2": 128}     # h columns of a Linear-1 tile
+L2_COLS = {"m1": 256, "m2": 256, "n1": 128, "n2": 256}    # y columns of a Linear-2 tile (d = 256)
 
 
-@pytest.mark.parametrize("mode", ["m1", "n2"])
+@pytest.mark.parametrize("mode", ["m1", "n1", "n2"])
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_ffn_parity(name, mode):
     need_gpu()
@@ -193,12 +196,12 @@ def test_ready_flags_carry_the_call_epoch(mode):
     s, ws, _, _ = run_ffn(c, tuning=t)
     tr = TILE_ROWS[mode]
     rows = int(sum((n + tr - 1) // tr for n in counts))  # scheduler rows
-    p2 = 1  # d = 256 -> one 256-wide Linear-2 tile per row
+    p2 = 256 // L2_COLS[mode]  # d = 256
     nflags = rows * p2 * cg  # one flag per CTA of each Linear-2 tile
     flags = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (nflags,)).cpu().numpy()
     assert flags[0] != 0 and np.all(flags == flags[0])
     done = moe.ws_view(ws, s, moe.WS.L1_DONE, torch.int32, (rows,)).cpu().numpy()
-    assert np.all(done == 2 * cg)  # F = 256 -> two Linear-1 tiles per row, one count per CTA
+    assert np.all(done == (256 // L1_COLS[mode]) * cg)  # F = 256: Linear-1 tiles per row, one count per CTA
     run_ffn(c, tuning=t, ws=ws)
     flags2 = moe.ws_view(ws, s, moe.WS.L2_FLAGS, torch.int32, (nflags,)).cpu().numpy()
     assert np.all(flags2 == flags2[0]) and flags2[0] != flags[0]

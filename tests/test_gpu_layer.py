@@ -121,6 +121,7 @@ FUSED_CASES = [custom_cfg(1000, 136, 5, 3, 200, S=8, zipf_s=2.0), custom_cfg(333
                custom_cfg(64, 512, 256, 8, 64), custom_cfg(1, 64, 4, 2, 64), custom_cfg(4096, 512, 8, 2, 256, S=4)]
 GEMM_MODES = {"m1": dict(cta_group=1, orientation=moe.ORIENT_TOKENS_M),
               "m2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_M),
+              "n1": dict(cta_group=1, orientation=moe.ORIENT_TOKENS_N),
               "n2": dict(cta_group=2, orientation=moe.ORIENT_TOKENS_N)}
 
 
