@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--h-ring", type=int, default=0,
                     help="h as a ring of this many scheduler rows (0 = every row in place)")
+    ap.add_argument("--l2-block-n", type=int, default=0, choices=[0, 64, 128, 192, 256],
+                    help="Linear-2 tile width with tokens on the M side (0 = default)")
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2],
                     help="CTAs per grouped-GEMM tile (0 = default)")
     ap.add_argument("--row-order", default="default", choices=["default", "expert", "mixed"],
@@ -332,7 +334,7 @@ def run_ours(args, cfg):
                         else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead, orientation=orient,
                         h_ring_rows=args.h_ring, fused_combine=1 if args.fused_combine else 0,
                         row_order={"default": 0, "expert": 1, "mixed": 2}[args.row_order],
-                        cta_group=args.cta_group)
+                        cta_group=args.cta_group, l2_block_n=args.l2_block_n)
     ws = moe.alloc_workspace(shape, dev, tuning if args.h_ring else None)
     rows = cfg.T // cfg.S
     out = [torch.empty(rows, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
@@ -517,6 +519,8 @@ def run_ours(args, cfg):
         line["config"]["orientation"] = args.orientation
     if args.cta_group:
         line["config"]["cta_group"] = args.cta_group
+    if args.l2_block_n:
+        line["config"]["l2_block_n"] = args.l2_block_n
     if args.row_order != "default":
         line["config"]["row_order"] = args.row_order
     if args.fused_combine:

@@ -168,10 +168,10 @@ struct SmemCtl {
 // bf16 (4 KiB); tokens on the N side two 2 KiB mailboxes and a 1 KiB slab
 constexpr int kEpiStageBytes = 5 * 1024;
 constexpr size_t kCtlBytes = (sizeof(SmemCtl) + 127) / 128 * 128;
-template <int CG>
+template <int CG, bool TN>
 constexpr size_t smem_bytes()
 {
-    return 1024 /*alignment slack*/ + size_t(Cfg<CG>::kStages) * (kATileBytes + Cfg<CG>::kBTileBytes) +
+    return 1024 /*alignment slack*/ + size_t(Cfg<CG, TN>::kStages) * (kATileBytes + Cfg<CG, TN>::kBTileBytes) +
            kCtlBytes + 4 * kEpiStageBytes;
 }
 
@@ -478,8 +478,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     extern __shared__ uint8_t smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
     uint8_t *sA = reinterpret_cast<uint8_t *>(base);
-    constexpr int kStages = Cfg<CG>::kStages;
-    constexpr int kBTileBytes = Cfg<CG>::kBTileBytes;
+    constexpr int kStages = Cfg<CG, TN>::kStages;
+    constexpr int kBTileBytes = Cfg<CG, TN>::kBTileBytes;
     constexpr int kTileRows = Cfg<CG, TN>::kTileRows;
     uint8_t *sB = sA + kStages * kATileBytes;
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(sB + kStages * kBTileBytes);
@@ -1126,12 +1126,16 @@ bool make_map_3d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t mid, 
 int ffn_l2_block_n(int d, int requested)
 {
     if (requested >= 64 && requested <= 256 && requested % 64 == 0) return requested;
-    // widest tile (multiple of 64) that wastes the fewest padded columns
+    // fewest tiles, then fewest padded columns: a k-block costs about the same
+    // for any tile width up to 256 (each new 128 x 64 A tile is read from shared
+    // memory at a fixed rate), so a narrower tile only adds k-blocks
     int best = 256;
-    long best_pad = LONG_MAX;
+    long best_tiles = LONG_MAX, best_pad = LONG_MAX;
     for (int n = 256; n >= 64; n -= 64) {
-        const long pad = static_cast<long>((d + n - 1) / n) * n - d;
-        if (pad < best_pad) {
+        const long tiles = (d + n - 1) / n;
+        const long pad = tiles * n - d;
+        if (tiles < best_tiles || (tiles == best_tiles && pad < best_pad)) {
+            best_tiles = tiles;
             best_pad = pad;
             best = n;
         }
@@ -1151,7 +1155,7 @@ namespace {
 template <int CG, bool TN, bool FC>
 cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
 {
-    constexpr size_t smem = smem_bytes<CG>();
+    constexpr size_t smem = smem_bytes<CG, TN>();
     static bool attr_set = false;
     static int max_instances = 0;
     const int sms = device_sm_count();
