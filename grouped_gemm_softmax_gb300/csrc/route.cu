@@ -407,7 +407,32 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     RouteParams p{a.x, a.wr, a.bias, a.topk_idx, a.topk_gate, a.T, a.d, a.E, a.k};
     // a block covers every expert (BE = 4*WE*TN >= E) and BT = 8*WT*TM tokens
     // <TM, TN, WE, WT, chunk>: measured best per expert count on GB300
-    if (a.E > 128) return launch_variant<8, 8, 8, 1, 32>(p, s);   // BT 64, BE 256
+    if (a.E > 128) {
+        // BE 256, one block of 256 threads per SM: pick the token tile (8 * TM
+        // tokens) whose last wave of blocks is fullest, slightly favouring
+        // larger tiles (more reuse of each staged feature chunk). fine
+        // (T = 16384, 152 SMs): TM = 7 gives 293 blocks = 1.93 waves, 11%
+        // faster than TM = 8 (256 blocks = 1.68 waves).
+        const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+        int best_tm = 8;
+        double best = -1.0;
+        for (int tm = 8; tm >= 5; --tm) {
+            const long blocks = (a.T + 8L * tm - 1) / (8L * tm);
+            const long slots = static_cast<long>(sms) * (tm <= 5 ? 2 : 1);  // TM 5: 128 registers, 2 blocks/SM
+            const long waves = (blocks + slots - 1) / slots;
+            const double score = static_cast<double>(blocks) / (waves * slots) * (1.0 - 0.02 * (8 - tm));
+            if (score > best) {
+                best = score;
+                best_tm = tm;
+            }
+        }
+        switch (best_tm) {
+        case 7: return launch_variant<7, 8, 8, 1, 32>(p, s);
+        case 6: return launch_variant<6, 8, 8, 1, 32>(p, s);
+        case 5: return launch_variant<5, 8, 8, 1, 32>(p, s);
+        default: return launch_variant<8, 8, 8, 1, 32>(p, s);
+        }
+    }
     if (a.E > 64) return launch_variant<2, 8, 4, 2, 64>(p, s);    // BT 32, BE 128
     if (a.E > 32) return launch_variant_async<2, 4, 4, 1, 128, 4>(p, s);  // BT 16, BE 64
     if (a.E > 16) return launch_variant<2, 2, 4, 2, 128>(p, s);           // BT 32, BE 32
