@@ -1127,8 +1127,8 @@ int ffn_l2_block_n(int d, int requested)
 {
     if (requested >= 64 && requested <= 256 && requested % 64 == 0) return requested;
     // fewest tiles, then fewest padded columns: a k-block costs about the same
-    // for any tile width up to 256 (each new 128 x 64 A tile is read from shared
-    // memory at a fixed rate), so a narrower tile only adds k-blocks
+    // for any tile width up to 256 (the loop is paced by delivering and issuing
+    // stages, not by the MMA width), so a narrower tile only adds k-blocks
     int best = 256;
     long best_tiles = LONG_MAX, best_pad = LONG_MAX;
     for (int n = 256; n >= 64; n -= 64) {
