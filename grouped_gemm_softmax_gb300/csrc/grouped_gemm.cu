@@ -1156,8 +1156,6 @@ template <int CG, bool TN, bool FC>
 cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
 {
     constexpr size_t smem = smem_bytes<CG, TN>();
-    static bool attr_set = false;
-    static int max_instances = 0;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
@@ -1173,20 +1171,44 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!attr_set) {
+    // once per device: the shared-memory attribute, and how many instances
+    // (CTAs or CTA pairs) can be resident at once -- every CTA of the
+    // persistent grid must be (the Linear-2 tiles wait on Linear-1 tiles of
+    // other CTAs)
+    struct Tag {};
+    static int max_inst[kOnceDevices];
+    auto init = [&](int dev) -> cudaError_t {
         cudaError_t err = cudaFuncSetAttribute(grouped_swiglu_gemm_kernel<CG, TN, FC>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
         if (err != cudaSuccess) return err;
-        // every CTA of the persistent grid must be resident at once (the
-        // Linear-2 tiles wait on Linear-1 tiles of other CTAs)
         int clusters = 0;
-        cfg.gridDim = dim3(static_cast<unsigned>(sms / CG * CG), 1, 1);
-        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG, TN, FC>, &cfg);
+        cudaLaunchConfig_t occ = cfg;
+        occ.gridDim = dim3(static_cast<unsigned>(sms / CG * CG), 1, 1);
+        err = cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG, TN, FC>, &occ);
+        if (err != cudaSuccess) return err;
+        const int m = clusters < sms / CG ? clusters : sms / CG;
+        if (m <= 0) return cudaErrorInvalidConfiguration;
+        if (dev >= 0 && dev < kOnceDevices) max_inst[dev] = m;
+        return cudaSuccess;
+    };
+    const cudaError_t ierr = once_per_device<Tag>(init);
+    if (ierr != cudaSuccess) return ierr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    int max_instances = 0;
+    if (dev >= 0 && dev < kOnceDevices) {
+        max_instances = max_inst[dev];
+    } else {
+        // no cached slot: query again (the attribute was set just now)
+        int clusters = 0;
+        cudaLaunchConfig_t occ = cfg;
+        occ.gridDim = dim3(static_cast<unsigned>(sms / CG * CG), 1, 1);
+        const cudaError_t err =
+            cudaOccupancyMaxActiveClusters(&clusters, grouped_swiglu_gemm_kernel<CG, TN, FC>, &occ);
         if (err != cudaSuccess) return err;
         max_instances = clusters < sms / CG ? clusters : sms / CG;
         if (max_instances <= 0) return cudaErrorInvalidConfiguration;
-        attr_set = true;
     }
     int instances = max_instances;
     if (a.num_ctas > 0) {

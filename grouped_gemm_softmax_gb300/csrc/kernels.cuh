@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 namespace moe {
@@ -117,5 +118,24 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 int device_sm_count();
+
+// Per-device one-time setup of a launch (kernel attributes, occupancy): the
+// first caller on a device runs init and every later caller on that device
+// gets its result. Thread safe; devices past kOnceDevices run init on every
+// call. Each distinct `Tag` type (one per kernel instantiation) has its own
+// state.
+constexpr int kOnceDevices = 64;
+template <typename Tag, typename Init>
+cudaError_t once_per_device(Init &&init)
+{
+    static std::once_flag flags[kOnceDevices];
+    static cudaError_t results[kOnceDevices];
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kOnceDevices) return init(dev);
+    std::call_once(flags[dev], [&] { results[dev] = init(dev); });
+    return results[dev];
+}
 
 }  // namespace moe

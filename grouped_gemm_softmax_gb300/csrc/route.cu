@@ -366,14 +366,12 @@ cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
     constexpr size_t stage = sizeof(float) * (kBK + 4) * (BT + BE);
     constexpr size_t logits = sizeof(float) * BT * (BE + 1);
     constexpr size_t smem = stage > logits ? stage : logits;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel<TM, TN, WE, WT, kBK>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    struct Tag {};
+    const cudaError_t e = once_per_device<Tag>([](int) {
+        return cudaFuncSetAttribute(route_kernel<TM, TN, WE, WT, kBK>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    });
+    if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
     return launch_pdl(route_kernel<TM, TN, WE, WT, kBK>, dim3(grid), dim3(NT), smem, s, p);
 }
@@ -387,14 +385,12 @@ cudaError_t launch_variant_async(const RouteParams &p, cudaStream_t s)
     constexpr size_t stage = sizeof(uint16_t) * STAGES * (BT + BE) * (KB + 8);
     constexpr size_t logits = sizeof(float) * BT * (BE + 1);
     constexpr size_t smem = stage > logits ? stage : logits;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel_async<TM, TN, WE, WT, KB, STAGES>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    struct Tag {};
+    const cudaError_t e = once_per_device<Tag>([](int) {
+        return cudaFuncSetAttribute(route_kernel_async<TM, TN, WE, WT, KB, STAGES>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    });
+    if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
     return launch_pdl(route_kernel_async<TM, TN, WE, WT, KB, STAGES>, dim3(grid), dim3(NT), smem, s, p);
 }
