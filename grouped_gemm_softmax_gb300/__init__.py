@@ -320,6 +320,7 @@ def last_device_status(ws, stream=None) -> int:
 
 
 def last_device_detail():
+    """(where, block, detail) of the last failure last_device_status read on this thread."""
     w, b, d = ctypes.c_uint32(), ctypes.c_uint32(), ctypes.c_uint32()
     library().moe_last_device_detail(ctypes.byref(w), ctypes.byref(b), ctypes.byref(d))
     return w.value, b.value, d.value

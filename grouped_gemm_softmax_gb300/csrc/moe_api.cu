@@ -128,7 +128,8 @@ uint32_t next_epoch()
     return e;
 }
 
-uint32_t g_detail[3] = {0, 0, 0};
+// detail words of the last device failure read by this thread
+thread_local uint32_t g_detail[3] = {0, 0, 0};
 
 moe_status_t check_tuning(const moe_tuning_t *t)
 {

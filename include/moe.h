@@ -290,8 +290,9 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
  * A failed CUDA call returns MOE_ERR_CUDA. */
 moe_status_t moe_last_device_status(void *ws, moe_stream_t stream);
 
-/* Detail words of the last device failure (valid after moe_last_device_status
- * returned non-OK): where (kernel/role code), block index, detail. */
+/* Detail words of the last device failure that moe_last_device_status read on
+ * the calling thread (valid after it returned non-OK there): where (kernel/role
+ * code), block index, detail. */
 void moe_last_device_detail(uint32_t *where, uint32_t *block, uint32_t *detail);
 
 #ifdef __cplusplus
