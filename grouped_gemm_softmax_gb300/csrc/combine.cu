@@ -57,9 +57,12 @@ combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ gate,
     float g[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-        // a slot whose expert id was out of range has no row (-1): no term
+        // a slot whose expert id was out of range has no row (-1): no term;
+        // neither has a row index past the T*k rows of y_perm
         const int r = j < k ? row_of_slot[t * k + j] : -1;
-        src[j] = r >= 0 ? reinterpret_cast<const uint4 *>(y + static_cast<long>(r) * d) : nullptr;
+        src[j] = (r >= 0 && r < static_cast<long>(T) * k)
+                     ? reinterpret_cast<const uint4 *>(y + static_cast<long>(r) * d)
+                     : nullptr;
         g[j] = j < k ? gate[t * k + j] : 0.0f;
     }
     uint4 *dst = reinterpret_cast<uint4 *>(seg.p[t / rows_per_seg] + (t % rows_per_seg) * static_cast<long>(d));

@@ -61,7 +61,9 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const moe
         return MOE_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm)) ||
         (reinterpret_cast<uintptr_t>(expert_counts) & 3u) ||
-        (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+        (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) ||
+        (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(row_of_slot) & 3u) ||
+        (reinterpret_cast<uintptr_t>(slot_of_row) & 3u))
         return MOE_ERR_INVALID_ARG;
 
     // the same chunking as moe_dispatch; it must fit the fixed scratch

@@ -292,7 +292,9 @@ moe_status_t moe_dispatch(const moe_shape_t *shape, const moe_bf16_t *x, const i
         return MOE_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm)) || !aligned16(ws) ||
         (reinterpret_cast<uintptr_t>(expert_counts) & 3u) ||
-        (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+        (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) ||
+        (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(row_of_slot) & 3u) ||
+        (reinterpret_cast<uintptr_t>(slot_of_row) & 3u))
         return MOE_ERR_INVALID_ARG;
     moe::DispatchArgs a{};
     a.x = x;
@@ -353,7 +355,9 @@ moe_status_t moe_combine(const moe_shape_t *shape, const moe_bf16_t *y_perm,
     if (st != MOE_OK) return st;
     if (shape->T == 0) return MOE_OK;
     if (!y_perm || !topk_gate || !row_of_slot || !out_segments) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_perm) || (reinterpret_cast<uintptr_t>(topk_gate) & 3u) ||
+        (reinterpret_cast<uintptr_t>(row_of_slot) & 3u))
+        return MOE_ERR_INVALID_ARG;
     moe::CombineArgs a{};
     for (int i = 0; i < shape->num_segments; ++i) {
         if (!out_segments[i] || !aligned16(out_segments[i])) return MOE_ERR_INVALID_ARG;

@@ -110,6 +110,23 @@ def test_null_pointers_and_small_workspace_are_rejected_on_the_host(lib):
                                     fake, nb, None) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_index_and_gate_arrays_must_be_4_byte_aligned(lib):
+    # the checks run before any launch: every other pointer is a fake, aligned address
+    s = moe.Shape(T=64, d=64, E=4, top_k=2, ffn=64)
+    c = ctypes.byref(s.c())
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    segs = (ctypes.c_void_p * 1)(1 << 21)
+    assert lib.moe_combine(c, fake, odd, fake, segs, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(c, fake, fake, odd, segs, None) == moe.MOE_ERR_INVALID_ARG
+    nb = moe.workspace_bytes(s)
+    for i in range(3):  # topk_idx, row_of_slot, slot_of_row
+        args = [fake, odd if i == 0 else fake, fake, fake, odd if i == 1 else fake,
+                odd if i == 2 else fake, fake, fake]
+        assert lib.moe_dispatch(c, *args, nb, None) == moe.MOE_ERR_INVALID_ARG
+        assert lib.moe_dispatch_noalloc(c, *args[:7], None) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_empty_call_enqueues_nothing(lib):
     s = moe.Shape(T=0, d=64, E=4, top_k=2, ffn=64)
     assert moe.workspace_bytes(s) > 0
