@@ -163,7 +163,9 @@ enum {
     MOE_WS_CHUNK_BASE = 10, /* dispatch scratch: [chunks,E] int32 */
     MOE_WS_L1_DONE = 11,    /* per scheduler row: finished Linear-1 tiles, u32; then per row the
                                finished Linear-2 tiles (used by the h ring) */
-    MOE_WS_L2_FLAGS = 12,   /* per Linear-2 tile: ready flag = epoch of the call that wrote it, u32 */
+    MOE_WS_L2_FLAGS = 12,   /* per Linear-2 tile: ready flag = epoch of the call that wrote it, u32
+                               (a call captured in a CUDA Graph keeps its capture-time epoch on
+                               every replay) */
     MOE_WS_NUM_REGIONS = 13
 };
 moe_status_t moe_workspace_region(const moe_shape_t *shape, int region, size_t *offset,

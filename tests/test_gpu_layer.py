@@ -94,6 +94,28 @@ def test_ragged_layers_every_token(cfg):
     _full_compare(layer, out, n_tokens=cfg.T, n_rows=cfg.R)
 
 
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], custom_cfg(333, 256, 33, 4, 128, S=3, zipf_s=1.0)],
+                         ids=["tiny", "T333_E33"])
+def test_layer_replays_from_a_cuda_graph(cfg):
+    """The layer only enqueues stream work (no allocation, no synchronisation),
+    so it can be captured once and replayed; every replay equals an eager call
+    bit for bit."""
+    need_gpu()
+    layer = GpuLayer(cfg, seed=2)
+    eager = layer.forward().clone()  # the eager call also does each launch's one-time setup
+    i = layer.inp
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, layer.ws)
+    for _ in range(3):
+        for o in layer.out:
+            o.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert moe.last_device_status(layer.ws) == moe.MOE_OK
+        assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), eager.view(torch.int16))
+
+
 def test_schedules_and_repeat_calls_are_bit_identical():
     need_gpu()
     layer = GpuLayer(synth.CONFIGS["tiny"])
