@@ -116,6 +116,22 @@ def test_layer_replays_from_a_cuda_graph(cfg):
         assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), eager.view(torch.int16))
 
 
+def test_first_calls_from_several_threads_at_once():
+    """The one-time per-device launch setup is thread safe: in a fresh process,
+    four threads start their first layer calls together (each with its own
+    stream, inputs and workspace) and all get the single-threaded result."""
+    need_gpu()
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join([os.path.dirname(here), here,
+                                                       os.environ.get("PYTHONPATH", "")]))
+    r = subprocess.run([sys.executable, os.path.join(here, "_concurrent_first_calls.py"), "4"],
+                       capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("ok")
+
+
 def test_schedules_and_repeat_calls_are_bit_identical():
     need_gpu()
     layer = GpuLayer(synth.CONFIGS["tiny"])
