@@ -91,6 +91,7 @@ constexpr int kL1N = 128;     // h columns per Linear-1 tile (MMA N = 2 * 128)
 constexpr int kATileBytes = kBlockM * kBlockK * 2;  // 16 KiB
 constexpr int kMaxStages = 6;
 constexpr int kDefaultGroupRows = 32;  // raster group, in 128-row M-tiles
+constexpr int kSmallExpertGroupRows = 16;  // ... when experts average under 4 scheduler rows
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr int kThreads = 192;
@@ -1311,7 +1312,13 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.wait_ns = a.wait_limit_us > 0 ? 1000ull * static_cast<unsigned long long>(a.wait_limit_us)
                                     : kWaitLimitNs;
     p.unmet_dependency = a.unmet_dependency > 0 ? 1 : 0;
-    const int group = a.group_rows > 0 ? a.group_rows : kDefaultGroupRows;  // 128-row M-tiles
+    // raster group (128-row M-tiles): with few rows per expert a smaller group
+    // keeps fewer experts' weight tiles in flight in L2 (fine, E = 256 with two
+    // 256-token rows per expert: 1.9-4% less GEMM time; with 8-16 rows per
+    // expert the default group is as fast or faster)
+    const long rows_per_expert = static_cast<long>(a.R) / (static_cast<long>(a.E) * 256);
+    const int group = a.group_rows > 0 ? a.group_rows
+                                       : (rows_per_expert < 4 ? kSmallExpertGroupRows : kDefaultGroupRows);
     p.group = (group + p.cg - 1) / p.cg;                                     // scheduler rows
     p.fc = a.gate != nullptr ? 1 : 0;
     if (p.fc) {

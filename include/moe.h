@@ -94,7 +94,9 @@ typedef struct {
     int l2_block_n; /* Linear-2 tile width (64, 128, 192 or 256) with tokens on the M side;
                        0 = default (ignored with tokens on the N side: 256) */
     int group_rows; /* raster group: an expert's tiles run N-tile-major over groups of this many
-                       128-row M-tiles, so each weight tile is reused while hot in L2; 0 = default */
+                       128-row M-tiles, so each weight tile is reused while hot in L2; 0 = default
+                       (16 when T*k/E < 1024, i.e. experts average under 4 rows of 256 tokens,
+                       else 32) */
     int cta_group;  /* CTAs per MMA tile: 2 = CTA pairs with 256-row tiles, 1 = single CTAs
                        with 128-row (tokens on M) or 128-weight-row (tokens on N) tiles;
                        0 = default (pairs, except tokens on the M side with T*k/E < 1024) */
