@@ -404,17 +404,19 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     // a block covers every expert (BE = 4*WE*TN >= E) and BT = 8*WT*TM tokens
     // <TM, TN, WE, WT, chunk>: measured best per expert count on GB300
     if (a.E > 128) {
-        // BE 256, one block of 256 threads per SM: pick the token tile (8 * TM
-        // tokens) whose last wave of blocks is fullest, slightly favouring
-        // larger tiles (more reuse of each staged feature chunk). fine
-        // (T = 16384, 152 SMs): TM = 7 gives 293 blocks = 1.93 waves, 11%
-        // faster than TM = 8 (256 blocks = 1.68 waves).
+        // BE 256 as 4 warps x 4 expert lanes x 16 experts per thread, 128
+        // threads and <= 255 registers, so two blocks share an SM. The token
+        // tile (8 * TM tokens) is the one whose last wave of blocks is
+        // fullest, slightly favouring larger tiles (more reuse of each staged
+        // feature chunk). fine (T = 16384, 152 SMs): TM = 7 gives 293 blocks,
+        // one wave of 304 slots, 801 us; the same tile with 8 experts per
+        // thread and 8 warps (one block per SM, two waves) took 828 us.
         const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+        const long slots = 2L * sms;
         int best_tm = 8;
         double best = -1.0;
-        for (int tm = 8; tm >= 5; --tm) {
+        for (int tm = 8; tm >= 4; --tm) {
             const long blocks = (a.T + 8L * tm - 1) / (8L * tm);
-            const long slots = static_cast<long>(sms) * (tm <= 5 ? 2 : 1);  // TM 5: 128 registers, 2 blocks/SM
             const long waves = (blocks + slots - 1) / slots;
             const double score = static_cast<double>(blocks) / (waves * slots) * (1.0 - 0.02 * (8 - tm));
             if (score > best) {
@@ -423,10 +425,11 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
             }
         }
         switch (best_tm) {
-        case 7: return launch_variant<7, 8, 8, 1, 32>(p, s);
-        case 6: return launch_variant<6, 8, 8, 1, 32>(p, s);
-        case 5: return launch_variant<5, 8, 8, 1, 32>(p, s);
-        default: return launch_variant<8, 8, 8, 1, 32>(p, s);
+        case 7: return launch_variant<7, 16, 4, 1, 32>(p, s);
+        case 6: return launch_variant<6, 16, 4, 1, 32>(p, s);
+        case 5: return launch_variant<5, 16, 4, 1, 32>(p, s);
+        case 4: return launch_variant<4, 16, 4, 1, 32>(p, s);
+        default: return launch_variant<8, 16, 4, 1, 32>(p, s);
         }
     }
     if (a.E > 64) return launch_variant<2, 8, 4, 2, 64>(p, s);    // BT 32, BE 128

@@ -32,10 +32,12 @@ def run_route(x, wr, bias, k):
     (256, 256, 8, 2, 0.0), (100, 64, 3, 2, 0.0), (1, 8, 1, 1, 0.0), (333, 136, 33, 5, 1.0),
     (130, 512, 64, 6, 1.0), (64, 1152, 16, 2, 1.2), (70, 256, 256, 8, 0.0), (65, 128, 200, 7, 0.5),
     (17, 32, 100, 4, 0.0), (4096, 2048, 64, 6, 1.0), (1000, 4096, 256, 8, 0.0), (129, 40, 128, 8, 0.0),
-    # E > 128 picks its token tile (8 * TM tokens, TM 5..8) from T for the fullest
-    # last wave; on 152 SMs these two take TM = 7 and TM = 5 (70 and 65 take 8,
-    # 1000 takes 6)
-    (8512, 64, 256, 8, 0.0), (12160, 64, 256, 8, 0.0),
+    # E > 128 picks its token tile (8 * TM tokens, TM 4..8) from T for the fullest
+    # last wave (two blocks per SM); on 152 SMs: 36 -> TM 4, 43 -> 5, 50 -> 6,
+    # 57 -> 7, 29 -> 8 (one block each), 12160 -> 5 and 8512 -> 4 (many blocks;
+    # the fine layer, T = 16384, takes 7)
+    (36, 64, 256, 8, 0.0), (43, 64, 256, 8, 0.0), (50, 64, 256, 8, 0.0), (57, 64, 256, 8, 0.0),
+    (29, 64, 256, 8, 0.0), (8512, 64, 256, 8, 0.0), (12160, 64, 256, 8, 0.0),
 ])
 def test_route_parity(T, d, E, k, zipf):
     need_gpu()
