@@ -58,6 +58,10 @@ CASES = {
     "dit_like_d": ([130, 5, 400], 1152, 384),
     "many_small_experts": ([3, 1, 0, 7, 130, 2, 0, 64] * 8, 128, 256),
     "one_row": ([1], 64, 64),
+    # the smallest widths the shape rules allow: feature and ffn widths of 8
+    # and 24/40, far below one 64-wide k-block (zero-filled past the end)
+    "min_widths": ([20, 5], 8, 8),
+    "small_widths": ([33, 0, 17], 24, 40),
 }
 
 

@@ -86,7 +86,8 @@ def test_tiny_layer_every_token():
 @pytest.mark.parametrize("cfg", [custom_cfg(1000, 136, 5, 3, 200, S=8, zipf_s=2.0),
                                  custom_cfg(333, 256, 33, 4, 128, S=3, zipf_s=1.0),
                                  custom_cfg(64, 512, 256, 8, 64),
-                                 custom_cfg(1, 64, 4, 2, 64)], ids=lambda c: f"T{c.T}_E{c.E}")
+                                 custom_cfg(1, 64, 4, 2, 64),
+                                 custom_cfg(50, 16, 6, 2, 24)], ids=lambda c: f"T{c.T}_E{c.E}_d{c.d}")
 def test_ragged_layers_every_token(cfg):
     need_gpu()
     layer = GpuLayer(cfg, seed=1)
