@@ -87,7 +87,12 @@ def test_tiny_layer_every_token():
                                  custom_cfg(333, 256, 33, 4, 128, S=3, zipf_s=1.0),
                                  custom_cfg(64, 512, 256, 8, 64),
                                  custom_cfg(1, 64, 4, 2, 64),
-                                 custom_cfg(50, 16, 6, 2, 24)], ids=lambda c: f"T{c.T}_E{c.E}_d{c.d}")
+                                 custom_cfg(50, 16, 6, 2, 24),
+                                 # 64 segments (the most allowed); top_k = E; almost every row on one expert
+                                 custom_cfg(128, 64, 8, 2, 64, S=64),
+                                 custom_cfg(40, 32, 8, 8, 64),
+                                 custom_cfg(2000, 64, 16, 1, 64, zipf_s=8.0)],
+                         ids=lambda c: f"T{c.T}_E{c.E}_k{c.k}_d{c.d}_S{c.S}")
 def test_ragged_layers_every_token(cfg):
     need_gpu()
     layer = GpuLayer(cfg, seed=1)
