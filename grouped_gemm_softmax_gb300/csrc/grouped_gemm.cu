@@ -153,6 +153,8 @@ struct SmemCtl {
     uint64_t estore[2];          // this CTA's epilogue stores issued (publisher)
     uint64_t drain;              // every MMA this CTA issued has completed (teardown)
     uint32_t tmem_base;
+    uint32_t p_uses;                 // stage loads this CTA's producer issued (teardown)
+    uint32_t p_bytes[kMaxStages];    // this CTA's bytes in the latest load of each stage
     int abort;
     int epi_fail;  // TN epilogue: a warp gave up (the warp pairs meet at barriers)
     int cunit;     // fused combine: next consumer unit of this CTA
@@ -468,6 +470,39 @@ __device__ bool combine_consumer(SmemCtl &c, const GemmParams &p, int lane, vola
     }
 }
 
+// Teardown, run by the producer thread of the pair's first CTA (or of a single
+// CTA) once both producers have stopped: wait until every stage load still in
+// flight has landed. Load i (of either CTA) used stage i mod S in phase
+// (i / S) mod 2, and a producer only issues load i after load i - S was
+// consumed, so only the last S loads can be in flight. With a pair, the two
+// producers may have stopped at different loads (each gives up on its own):
+// a stage the first CTA armed for both halves but the peer never loaded gets
+// the peer's bytes counted here, and a stage only the peer loaded gets its
+// arrival and byte count here, so every such phase completes once the issued
+// copies land. A wait that runs out is recorded in the status word.
+template <int CG, int kStages>
+__device__ void drain_loads(SmemCtl &c, const GemmParams &p)
+{
+    constexpr unsigned long long kDrainLimitNs = 50000000ull;
+    const uint32_t own = c.p_uses;
+    uint32_t peer = own;
+    if constexpr (CG == 2) peer = ld_shared_cluster_u32(map_to_cta(smem_u32(&c.p_uses), 1));
+    const uint32_t n = own > peer ? own : peer;
+    const uint32_t lo = n > static_cast<uint32_t>(kStages) ? n - kStages : 0u;
+    for (uint32_t i = lo; i < n; ++i) {
+        const int s = static_cast<int>(i % kStages);
+        const uint32_t par = (i / kStages) & 1u;
+        if constexpr (CG == 2) {
+            if (i < own && i >= peer)
+                mbar_complete_tx(&c.full[s], c.p_bytes[s]);
+            else if (i >= own && i < peer)
+                mbar_arrive_expect_tx(&c.full[s], ld_shared_cluster_u32(map_to_cta(smem_u32(&c.p_bytes[s]), 1)));
+        }
+        if (!mbar_wait_drain(&c.full[s], par, kDrainLimitNs))
+            report_failure(p.status, kStatusTimeout, kWhereLoadDrain, static_cast<unsigned>(s));
+    }
+}
+
 template <int CG, bool TN, bool FC>
 __global__ void __launch_bounds__(FC ? kThreads + kConsumerThreads : kThreads, 1)
 grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -506,6 +541,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             mbar_init(&c.estore[b], kEpiThreads);
         }
         mbar_init(&c.drain, 1);
+        c.p_uses = 0;
         c.abort = 0;
         c.epi_fail = 0;
         c.cunit = 0;
@@ -656,6 +692,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             Scheduler sch(c, p);
             int s = 0;
             uint32_t ph = 0;
+            uint32_t uses = 0;
             bool ok = true;
             unsigned long long w_empty = 0, w_rows = 0, t0 = tr ? clock64() : 0;
             for (int tl = 0; ok; ++tl) {
@@ -746,12 +783,15 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         tma_load_3d<CG>(&tm_w2, bar, b, kb * kBlockK,
                                         t.n * p.N2 + static_cast<int>(rank) * (p.N2 / CG), e);
                     }
+                    c.p_bytes[s] = bytes / CG;
+                    ++uses;
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
             }
+            c.p_uses = uses;
             if (tr) {
                 unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
                 o[0] = w_empty;
@@ -833,7 +873,8 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             // every issued MMA must finish before tensor memory is freed, also
             // when the loop was left early
             mma_commit<CG>(&c.drain, 1);
-            mbar_wait_drain(&c.drain, 0, p.wait_ns);
+            if (!mbar_wait_drain(&c.drain, 0, p.wait_ns))
+                report_failure(p.status, kStatusTimeout, kWhereMmaDrain, static_cast<unsigned>(s));
             if (tr) {
                 unsigned long long *o = p.trace + blockIdx.x * kTraceWords;
                 o[3] = w_full;
@@ -1079,15 +1120,16 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
     }
 
-    // after an early exit, let loads that were already issued land before the
-    // CTA's shared memory is released (bounded; never taken on the normal path)
-    if (warp == 0 && lane == 0 && (*abort_flag || ld_volatile_u32(p.status) != 0u)) {
-        const unsigned long long t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
-    }
     tc_fence_before();
     __syncthreads();
-    if constexpr (CG == 2) cluster_sync_all();  // the pair is done with both CTAs' tensor memory
+    if constexpr (CG == 2) cluster_sync_all();  // both producers have stopped issuing loads
+    // every TMA load the CTA (pair) issued has landed before its shared memory
+    // is released: on the normal path the MMA thread consumed them all and
+    // these waits return at once; after an early exit they cover the loads
+    // still in flight
+    if (warp == 0 && lane == 0 && leader) drain_loads<CG, kStages>(c, p);
+    __syncwarp();
+    if constexpr (CG == 2) cluster_sync_all();  // the peer stays until its loads have landed too
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, kTmemCols);

@@ -17,7 +17,8 @@ namespace moe {
 enum : unsigned { kStatusBadExpert = 1u, kStatusBadOffsets = 1u, kStatusTimeout = 5u };
 enum : unsigned {
     kWhereProducerEmpty = 1, kWhereProducerDep = 2, kWhereMmaFull = 3, kWhereMmaTmemEmpty = 4,
-    kWhereEpiTmemFull = 5, kWhereDispatch = 6, kWhereGemmOffsets = 7, kWhereCombine = 8
+    kWhereEpiTmemFull = 5, kWhereDispatch = 6, kWhereGemmOffsets = 7, kWhereCombine = 8,
+    kWhereMmaDrain = 9, kWhereLoadDrain = 10
 };
 
 // Default wall-clock limit of any single wait (ns). The longest legitimate
@@ -73,6 +74,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
+                 : "memory");
+}
+
+// Count `bytes` as delivered without a copy (the teardown path, for a stage
+// whose other half was never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
 
@@ -207,6 +216,14 @@ __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                      "memory");
+}
+
+// 32-bit load from a shared::cluster address (another CTA's shared memory)
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 // arrive on an mbarrier that may live in another CTA of the cluster

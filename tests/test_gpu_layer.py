@@ -125,7 +125,8 @@ def test_layer_replays_from_a_cuda_graph(cfg):
 def test_first_calls_from_several_threads_at_once():
     """The one-time per-device launch setup is thread safe: in a fresh process,
     four threads start their first layer calls together (each with its own
-    stream, inputs and workspace) and all get the single-threaded result."""
+    inputs and workspace, on one shared stream, since two grouped GEMMs must
+    not run on the device at once) and all get the single-threaded result."""
     need_gpu()
     import subprocess
     import sys
