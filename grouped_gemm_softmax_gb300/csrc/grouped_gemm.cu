@@ -23,10 +23,9 @@
 // holds Q scheduler rows instead of all of them; row p lives in slot p mod Q.
 // A Linear-1 tile of row p >= Q first waits (acquire, bounded) until every
 // Linear-2 tile of row p - Q has finished (l2_done[p - Q] = CTAs per tile *
-// P2), so the slot's previous rows have been read. With Q >= D + group + 1
-// every such Linear-2 tile sits before the waiting tile in every instance's
-// sequence (an instance emits all its Linear-2 tiles of row r before any
-// Linear-1 tile past row r + D), so these waits cannot deadlock either.
+// P2), so the slot's previous rows have been read. With Q >= D + 2 * group
+// every such Linear-2 tile comes earlier in the tile order than the waiting
+// tile (see TileSource), so these waits cannot deadlock either.
 //
 // Fused combine (FC; Cui et al., section 3.3: a consumer polls the producer's
 // per-tile signals and sends each finished block to its owner): two more warps
@@ -38,15 +37,16 @@
 // never wait on them, and the fp32 sum runs in j order exactly as the combine
 // kernel's, so the output bits are the same.
 //
-// Order (Xian et al., Algorithm 1, read for unpaired CTAs): CTA g of G walks two
-// cursors k1, k2 (start g, step G) over the Linear-1 and Linear-2 tile streams
-// (row-major over (row, n)); it emits the Linear-2 tile at k2 when its row
+// Order (Xian et al., Algorithm 1): one cursor pair k1, k2 walks the Linear-1
+// and Linear-2 tile streams; the Linear-2 tile at k2 goes out once its row
 // trails the Linear-1 cursor's row by at least D, else the next Linear-1 tile.
-// With D >= 1 every Linear-2 tile waits only on Linear-1 tiles of earlier
-// positions in every CTA's sequence, so the waits cannot deadlock (all CTAs
-// are co-resident: grid <= SM count, one CTA per SM). The expert-wave order
-// (all Linear-1 tiles of a wave of experts, then its Linear-2 tiles) is kept
-// as the comparison schedule. Both orders give bit-identical outputs.
+// That gives ONE global tile sequence; the instances (CTAs or CTA pairs) take
+// its tiles in order from a global ticket counter, so every tile is started
+// by a CTA that is running, every dependency wait is on a tile with a smaller
+// ticket, and the waits cannot deadlock whether or not the whole grid is
+// resident (see TileSource). The expert-wave order (all Linear-1 tiles of a
+// wave of experts, then its Linear-2 tiles) is kept as the comparison
+// schedule. Both orders give bit-identical outputs.
 //
 // CTA roles (192 threads, 256 with the fused combine): warp 0 = TMA producer,
 // warp 1 = tensor-memory allocator + single-thread MMA issuer, warps 2..5 =
@@ -105,6 +105,7 @@ constexpr int kTraceWords = 16;  // per-CTA counters when tracing is on
 // 7 epilogue stores done
 constexpr int kTileTraceWords = 8;
 constexpr int kMaxMixedRows = 1024;  // scheduler rows the mixed order can hold
+constexpr int kTileQueue = 8;        // tile descriptors in flight per CTA
 constexpr bool kMixedByDefault = true;
 
 template <int CG, bool TN = false>
@@ -122,6 +123,7 @@ struct GemmParams {
     uint16_t *y;
     unsigned *l1_done;
     unsigned *l2_done;  // per scheduler row: finished Linear-2 tiles (h ring only)
+    unsigned *ticket;   // next tile of the global order (zero at launch)
     unsigned *l2_flags;
     unsigned *status;
     int E, d, F, R;
@@ -152,6 +154,10 @@ struct SmemCtl {
     uint64_t tempty[2];          // accumulator drained (every epilogue thread of the pair)
     uint64_t estore[2];          // this CTA's epilogue stores issued (publisher)
     uint64_t drain;              // every MMA this CTA issued has completed (teardown)
+    uint64_t tq_full[kTileQueue];   // descriptor written (in each CTA of the pair)
+    uint64_t tq_empty[kTileQueue];  // descriptor read by every reading role (in the CTA that publishes)
+    uint64_t sched_go;              // pair scheduler: this CTA's producer took a descriptor
+    int4 tq[kTileQueue];            // tile descriptors (pack_tile)
     uint32_t tmem_base;
     uint32_t p_uses;                 // stage loads this CTA's producer issued (teardown)
     uint32_t p_bytes[kMaxStages];    // this CTA's bytes in the latest load of each stage
@@ -164,7 +170,8 @@ struct SmemCtl {
     int wave_row[kMaxExperts + 1];   // wave w spans scheduler rows [wave_row[w], wave_row[w+1])
     int wave_tile[kMaxExperts + 1];  // first global tile index of wave w
     int mixed;                       // scheduler rows in the mixed order (mrow) instead of expert order
-    int mrow[kMaxMixedRows];         // mixed order: scheduler row -> expert | band << 9
+    int mrow[kMaxMixedRows];         // scheduler row -> expert | band << 9 (when the rows fit)
+    int seg[kMaxMixedRows + 1];      // first ticket of each row block's segment (interleaved order)
 };
 
 // epilogue buffer per epilogue warp: tokens on the M side use 32 rows x 64
@@ -178,6 +185,9 @@ constexpr size_t smem_bytes()
            kCtlBytes + 4 * kEpiStageBytes;
 }
 
+static_assert(smem_bytes<2, true>() <= 232448 && smem_bytes<1, false>() <= 232448,
+              "shared memory of the grouped GEMM exceeds 227 KiB");
+
 struct Tile {
     int kind;  // 0 = Linear-1, 1 = Linear-2, -1 = no more tiles
     int row;   // scheduler row
@@ -190,113 +200,175 @@ struct Tile {
 // of one expert occupy positions [row_start[e]*Pn, row_start[e+1]*Pn); inside
 // the expert they run over groups of GM consecutive rows, N-tile-major within a
 // group, so a weight tile is reused by the group's M-tiles back to back. Every
-// tile of row p sits below position (p + GM) * Pn. A CTA only ever asks for
-// increasing positions of a stream, so the expert is found by advancing a
-// cursor (32-bit arithmetic: this runs on the MMA thread between tiles).
-struct StreamCursor {
-    int e = 0;
-
-    __device__ Tile at(const SmemCtl &c, int E, int k, int Pn, int GM, int kind, int rows)
-    {
-        Tile t;
-        t.kind = kind;
-        const int per_group = GM * Pn;
-        if (c.mixed) {
-            // mixed order: the raster groups run over the global row sequence
-            const int P = c.row_start[E];
-            const int j = k / per_group;
-            const int gs = min(GM, P - j * GM);
-            const int i = k - j * per_group;
-            t.n = i / gs;
-            t.row = j * GM + i % gs;
-            const int packed = c.mrow[t.row];
-            t.e = packed & 0x1FF;
-            t.b0 = c.offs[t.e] + (packed >> 9) * rows;
-            return t;
-        }
-        while (e + 1 < E && c.row_start[e + 1] * Pn <= k) ++e;
-        t.e = e;
-        const int r0 = c.row_start[e];
-        const int local = k - r0 * Pn;
-        const int j = local / per_group;
-        const int gs = min(GM, c.row_start[e + 1] - r0 - j * GM);
-        const int i = local - j * per_group;
-        t.n = i / gs;
-        t.row = r0 + j * GM + i % gs;
-        t.b0 = c.offs[e] + (t.row - r0) * rows;
-        return t;
+// tile of row p sits below position (p + GM) * Pn and at or above position
+// (p - GM + 1) * Pn. In the mixed order the groups run over the global row
+// sequence instead.
+__device__ __forceinline__ int expert_of_row(const SmemCtl &c, int E, int row)
+{
+    if (c.row_start[E] <= kMaxMixedRows) return c.mrow[row] & 0x1FF;  // the table holds every row
+    // the largest e with row_start[e] <= row (row < row_start[E]): experts
+    // without rows share their row_start with the next expert
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (c.row_start[mid] <= row) lo = mid;
+        else hi = mid - 1;
     }
-};
+    return lo;
+}
 
-// Every role of a CTA runs its own copy of this deterministic walk, so they all
-// see the same tile sequence without communicating.
-struct Scheduler {
-    int k1, k2, tot1, tot2;
-    int gi;
-    int w;
-    int P1, P2, G, D, GM, mode, rows;
-    StreamCursor s1, s2;
-    Tile t2;         // decoded Linear-2 tile at k2 (interleaved mode)
-    bool t2_valid;
+// first row and size of the raster group holding scheduler row m
+__device__ __forceinline__ void group_of_row(const SmemCtl &c, int E, int GM, int m, int &g0, int &gs)
+{
+    if (c.mixed) {
+        g0 = m - m % GM;
+        gs = min(GM, c.row_start[E] - g0);
+        return;
+    }
+    const int e = expert_of_row(c, E, m);
+    const int r0 = c.row_start[e];
+    g0 = m - (m - r0) % GM;
+    gs = min(GM, c.row_start[e + 1] - g0);
+}
 
-    __device__ Scheduler(const SmemCtl &c, const GemmParams &p)
+__device__ Tile stream_tile(const SmemCtl &c, int E, int k, int Pn, int GM, int kind, int rows)
+{
+    Tile t;
+    t.kind = kind;
+    int g0, gs;
+    group_of_row(c, E, GM, k / Pn, g0, gs);  // positions of a group: [g0 * Pn, (g0 + gs) * Pn)
+    const int i = k - g0 * Pn;
+    t.n = i / gs;
+    t.row = g0 + i % gs;
+    if (c.mixed || c.row_start[E] <= kMaxMixedRows) {
+        const int packed = c.mrow[t.row];
+        t.e = packed & 0x1FF;
+        t.b0 = c.offs[t.e] + (packed >> 9) * rows;
+    } else {
+        t.e = expert_of_row(c, E, t.row);
+        t.b0 = c.offs[t.e] + (t.row - c.row_start[t.e]) * rows;
+    }
+    return t;
+}
+
+// The tile order (Xian et al., Algorithm 1, taken as ONE sequence for the
+// whole grid). Instances claim tickets 0, 1, 2, ... from a global counter, so
+// every tile is started by a running CTA and in ticket order. Interleaved
+// schedule: the Linear-1 and Linear-2 streams merged with lead D, i.e. the
+// sequence one instance walking both streams with step 1 would emit. With
+// m(k2) the largest row among Linear-2 positions <= k2 (the stream is in
+// order, so a tile never passes an earlier one), the Linear-2 tile at k2 goes
+// right before the Linear-1 tiles of row block K = min(m(k2) + D, P), or after
+// all of them when K = P. The sequence is thus, for b = 0 .. P: the Linear-2
+// tiles with K = b, then the P1 Linear-1 tiles of block b. Segment b starts at
+// ticket S(b) = b * P1 + C(b - D - 1), C(m) = number of Linear-2 positions
+// with m(k2) <= m (a closed form per raster group), so a ticket is decoded by
+// a binary search over b.
+//   Dependencies: a Linear-2 tile of row r waits for the Linear-1 tiles of
+// row r, all in blocks < r + GM <= r + D <= K when D >= GM; a Linear-1 tile
+// of row p in an h ring of Q rows waits for the Linear-2 tiles of row p - Q,
+// whose K <= p - Q + GM - 1 + D <= p - GM + 1 (the first block holding
+// tiles of row p) when Q >= D + 2 GM. So every wait is on a smaller ticket,
+// claimed earlier by a CTA that is running, and the waits cannot deadlock
+// however many CTAs are resident.
+// Expert-wave schedule: ticket = position in the wave sequence (each wave:
+// its Linear-1 tiles, then its Linear-2 tiles).
+struct TileSource {
+    int P, P1, P2, D, GM, mode, rows, tot1, tot2, E;
+
+    __device__ TileSource(const SmemCtl &c, const GemmParams &p)
     {
-        const int P = c.row_start[p.E];
+        P = c.row_start[p.E];
         P1 = p.P1;
         P2 = p.P2;
-        G = gridDim.x / p.cg;
         D = p.lead;
         GM = p.group;
         mode = p.schedule;
-        rows = p.rows;  // token rows of one scheduler row
-        k1 = k2 = blockIdx.x / p.cg;
+        rows = p.rows;
         tot1 = P * P1;
         tot2 = P * P2;
-        gi = blockIdx.x / p.cg;
-        w = 0;
-        t2_valid = false;
+        E = p.E;
     }
 
-    __device__ Tile next(const SmemCtl &c, int E)
+    // C(m): Linear-2 positions whose largest row so far is <= m. Inside a
+    // raster group (g0, gs) the first pass (n = 0) walks its rows one by
+    // one, every later pass already holds the group's last row.
+    __device__ int l2_count(const SmemCtl &c, int m) const
+    {
+        if (m < 0) return 0;
+        if (m >= P - 1) return tot2;
+        int g0, gs;
+        group_of_row(c, E, GM, m, g0, gs);
+        return m < g0 + gs - 1 ? g0 * P2 + (m - g0 + 1) : (g0 + gs) * P2;
+    }
+
+    __device__ Tile decode(const SmemCtl &c, unsigned q) const
     {
         Tile t;
-        if (mode == 0) {
-            // Algorithm 1: the Linear-1 cursor sits at row floor(k1 / P1); a
-            // Linear-2 tile goes out once its row trails that by D >= GM rows.
-            if (k1 >= tot1 && k2 >= tot2) {
+        if (mode != 0) {
+            if (q >= static_cast<unsigned>(c.wave_tile[c.nwaves])) {
                 t.kind = -1;
                 return t;
             }
-            const int p1 = (k1 < tot1) ? k1 / P1 : INT_MAX / 2;
-            if (k2 < tot2) {
-                if (!t2_valid) {
-                    t2 = s2.at(c, E, k2, P2, GM, 1, rows);
-                    t2_valid = true;
-                }
-                if (t2.row + D <= p1) {
-                    k2 += G;
-                    t2_valid = false;
-                    return t2;
-                }
+            const int gi = static_cast<int>(q);
+            int lo = 0, hi = c.nwaves - 1;  // the wave holding gi
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (c.wave_tile[mid] <= gi) lo = mid;
+                else hi = mid - 1;
             }
-            t = s1.at(c, E, k1, P1, GM, 0, rows);
-            k1 += G;
-            return t;
+            const int j = gi - c.wave_tile[lo];
+            const int r0 = c.wave_row[lo];
+            const int nr = c.wave_row[lo + 1] - r0;
+            if (j < nr * P1) return stream_tile(c, E, r0 * P1 + j, P1, GM, 0, rows);
+            return stream_tile(c, E, r0 * P2 + (j - nr * P1), P2, GM, 1, rows);
         }
-        // expert waves: all Linear-1 tiles of a wave, then its Linear-2 tiles
-        if (gi >= c.wave_tile[c.nwaves]) {
+        if (q >= static_cast<unsigned>(tot1 + tot2)) {
             t.kind = -1;
             return t;
         }
-        while (gi >= c.wave_tile[w + 1]) ++w;
-        const int j = gi - c.wave_tile[w];
-        const int r0 = c.wave_row[w];
-        const int nr = c.wave_row[w + 1] - r0;
-        gi += G;
-        if (j < nr * P1) return s1.at(c, E, r0 * P1 + j, P1, GM, 0, rows);
-        return s2.at(c, E, r0 * P2 + (j - nr * P1), P2, GM, 1, rows);
+        const int qi = static_cast<int>(q);
+        // the segment holding ticket q: the largest b in [0, P] with S(b) <= q
+        int lo = 0, hi = P;
+        if (P <= kMaxMixedRows) {
+            while (lo < hi) {  // over the table the prologue built
+                const int mid = (lo + hi + 1) >> 1;
+                if (c.seg[mid] <= qi) lo = mid;
+                else hi = mid - 1;
+            }
+        } else {
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (mid * P1 + l2_count(c, mid - D - 1) <= qi) lo = mid;
+                else hi = mid - 1;
+            }
+        }
+        const int b = lo;
+        const int c0 = l2_count(c, b - D - 1);
+        const int n2 = (b < P ? l2_count(c, b - D) : tot2) - c0;  // Linear-2 tiles of the segment
+        const int off = qi - (b * P1 + c0);
+        if (off < n2) return stream_tile(c, E, c0 + off, P2, GM, 1, rows);
+        return stream_tile(c, E, b * P1 + (off - n2), P1, GM, 0, rows);
     }
 };
+
+// Tile descriptors pass from the producer that claims them to the CTA's other
+// roles (and the peer CTA) through a small shared-memory queue.
+__device__ __forceinline__ int4 pack_tile(const Tile &t)
+{
+    return make_int4(t.kind < 0 ? -1 : (t.kind | (t.n << 1)), t.row, t.e, t.b0);
+}
+
+__device__ __forceinline__ Tile unpack_tile(int4 v)
+{
+    Tile t;
+    t.kind = v.x < 0 ? -1 : (v.x & 1);
+    t.n = v.x < 0 ? 0 : (v.x >> 1);
+    t.row = v.y;
+    t.e = v.z;
+    t.b0 = v.w;
+    return t;
+}
 
 __device__ __forceinline__ bool wait_rows_ready(const unsigned *ctr, unsigned target,
                                                 volatile int *cta_abort, unsigned *status,
@@ -480,6 +552,55 @@ __device__ bool combine_consumer(SmemCtl &c, const GemmParams &p, int lane, vola
 // the peer's bytes counted here, and a stage only the peer loaded gets its
 // arrival and byte count here, so every such phase completes once the issued
 // copies land. A wait that runs out is recorded in the status word.
+// Publish the tile of a claimed ticket as descriptor number tl: single CTA:
+// by its producer; pair: by the second CTA's scheduler thread, into both CTAs'
+// queues (`other` = the other CTA's rank). False when the wait for a free
+// queue slot gave up.
+template <int CG>
+__device__ bool publish_tile(SmemCtl &c, const GemmParams &p, const TileSource &src, int tl, unsigned ticket,
+                             Tile &out, volatile int *abort_flag, uint32_t other)
+{
+    const int q = tl % kTileQueue;
+    const uint32_t ph = static_cast<uint32_t>(tl / kTileQueue) & 1u;
+    out = src.decode(c, ticket);
+    if (!mbar_wait_cluster(&c.tq_empty[q], ph ^ 1u, abort_flag, p.status, kWhereTileQueue,
+                           static_cast<unsigned>(tl), p.wait_ns))
+        return false;
+    const int4 v = pack_tile(out);
+    c.tq[q] = v;
+    if constexpr (CG == 2) {
+        st_shared_cluster_v4(map_to_cta(smem_u32(&c.tq[q]), other), v);
+        mbar_arrive_cluster(map_to_cta(smem_u32(&c.tq_full[q]), other));
+    }
+    mbar_arrive(&c.tq_full[q]);
+    return true;
+}
+
+// Every other role: wait for descriptor number tl and read it. False when
+// the wait gave up.
+__device__ __forceinline__ bool take_tile(SmemCtl &c, const GemmParams &p, int tl, Tile &out,
+                                          volatile int *abort_flag)
+{
+    const int q = tl % kTileQueue;
+    const uint32_t ph = static_cast<uint32_t>(tl / kTileQueue) & 1u;
+    if (!mbar_wait_cluster(&c.tq_full[q], ph, abort_flag, p.status, kWhereTileQueue,
+                           0x10000000u | static_cast<unsigned>(tl), p.wait_ns))
+        return false;
+    out = unpack_tile(c.tq[q]);
+    return true;
+}
+
+// Give descriptor tl's queue slot back (once per reading role, after every
+// thread of the role has read it). The slots are counted where the publisher
+// runs: the single CTA, or the second CTA of a pair.
+template <int CG>
+__device__ __forceinline__ void release_tile(SmemCtl &c, int tl, uint32_t rank)
+{
+    const int q = tl % kTileQueue;
+    if (CG == 1 || rank == 1) mbar_arrive(&c.tq_empty[q]);
+    else mbar_arrive_cluster(map_to_cta(smem_u32(&c.tq_empty[q]), 1));
+}
+
 template <int CG, int kStages>
 __device__ void drain_loads(SmemCtl &c, const GemmParams &p)
 {
@@ -541,6 +662,15 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
             mbar_init(&c.estore[b], kEpiThreads);
         }
         mbar_init(&c.drain, 1);
+        for (int q = 0; q < kTileQueue; ++q) {
+            mbar_init(&c.tq_full[q], 1);
+            // readers of a descriptor: single CTA: the MMA thread and the four
+            // epilogue warps (the producer publishes); pair: both producers, the
+            // MMA thread and both CTAs' epilogue warps (the peer's scheduler
+            // thread publishes)
+            mbar_init(&c.tq_empty[q], CG == 2 ? 11 : 5);
+        }
+        mbar_init(&c.sched_go, 1);
         c.p_uses = 0;
         c.abort = 0;
         c.epi_fail = 0;
@@ -656,7 +786,21 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 }
             }
         }
+        if (!mixed && !any_bad && c.row_start[E] <= kMaxMixedRows) {
+            // expert order: the same row table, read by the tile decode
+            for (int i = 0; i < per; ++i) {
+                const int e = lane * per + i;
+                if (e >= E) break;
+                for (int r = c.row_start[e]; r < c.row_start[e + 1]; ++r) c.mrow[r] = e | ((r - c.row_start[e]) << 9);
+            }
+        }
         if (lane == 0) c.mixed = mixed;
+        __syncwarp();
+        if (p.schedule == 0 && c.row_start[E] <= kMaxMixedRows) {
+            // segment starts of the interleaved tile order, S(b) for b = 0 .. P
+            const TileSource src(c, p);
+            for (int b = lane; b <= src.P; b += 32) c.seg[b] = b * src.P1 + src.l2_count(c, b - src.D - 1);
+        }
         __syncwarp();
         if (lane == 0) {
             // expert waves for the comparison schedule: consecutive experts until
@@ -689,14 +833,30 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            Scheduler sch(c, p);
+            const TileSource src(c, p);
             int s = 0;
             uint32_t ph = 0;
             uint32_t uses = 0;
             bool ok = true;
             unsigned long long w_empty = 0, w_rows = 0, t0 = tr ? clock64() : 0;
+            // A single CTA claims and publishes the next tile itself, once a
+            // few stages of the current one are queued (the claim and its
+            // decode then overlap the wait for free stages). In a pair both
+            // producers take the tiles the second CTA's scheduler thread
+            // publishes, off this thread's path.
+            Tile next;
+            unsigned claimed = 0;  // single CTA: ticket of the next tile, claimed at the current tile's first stage
+            if (CG == 1) ok = publish_tile<CG>(c, p, src, 0, atomicAdd(p.ticket, 1u), next, abort_flag, 0u);
             for (int tl = 0; ok; ++tl) {
-                const Tile t = sch.next(c, E);
+                Tile t;
+                if (CG == 1) {
+                    t = next;
+                } else if (take_tile(c, p, tl, t, abort_flag)) {
+                    release_tile<CG>(c, tl, rank);
+                    if (rank == 1) mbar_arrive(&c.sched_go);  // the scheduler may publish the next one
+                } else {
+                    break;
+                }
                 if (t.kind < 0) break;
                 unsigned long long *rec =
                     (p.tile_trace && tl < p.tile_trace_cap)
@@ -789,6 +949,15 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                         s = 0;
                         ph ^= 1u;
                     }
+                    if constexpr (CG == 1) {
+                        // the atomic's result is only needed a few stages later
+                        if (kb == 0) claimed = atomicAdd(p.ticket, 1u);
+                        if (kb == min(3, nkb - 1) &&
+                            !publish_tile<CG>(c, p, src, tl + 1, claimed, next, abort_flag, 0u)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                 }
             }
             c.p_uses = uses;
@@ -802,16 +971,15 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
-            Scheduler sch(c, p);
             int s = 0;
             uint32_t ph = 0;
             const uint32_t idesc1 = idesc_bf16_f32(kTileRows, 2 * kL1N);
             const uint32_t idesc2 = idesc_bf16_f32(kTileRows, p.N2);
             bool ok = true;
             unsigned long long w_full = 0, w_tmem = 0, t0 = tr ? clock64() : 0;
-            // the next tile is worked out while the current tile's first MMAs
-            // run, so the tensor pipe does not idle between tiles
-            Tile t_next = sch.next(c, E);
+            Tile t_next;
+            ok = take_tile(c, p, 0, t_next, abort_flag);
+            if (ok) release_tile<CG>(c, 0, rank);
             for (int tl = 0; ok; ++tl) {
                 const Tile t = t_next;
                 if (t.kind < 0) break;
@@ -858,10 +1026,17 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                                         (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit<CG>(&c.empty[s]);
-                    if (kb == 0) t_next = sch.next(c, E);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
+                    }
+                    if (kb == nkb - 1) {
+                        // the next descriptor, read while this tile's last MMAs run
+                        if (!take_tile(c, p, tl + 1, t_next, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        release_tile<CG>(c, tl + 1, rank);
                     }
                 }
                 if (rec) {
@@ -881,6 +1056,22 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 o[4] = w_tmem;
                 o[5] = clock64() - t0;
             }
+        } else if (CG == 2 && lane == 0) {
+            // ------------------------------------------------------------ pair scheduler
+            // The second CTA's MMA warp, otherwise idle, claims the tickets and
+            // publishes their tiles to both CTAs: tile tl + 1 once this CTA's
+            // producer has taken tile tl, so both producers find it long
+            // before they need it and neither spends time on the claim.
+            const TileSource src(c, p);
+            for (int tl = 0;; ++tl) {
+                if (tl > 0 && !mbar_wait_cluster(&c.sched_go, static_cast<uint32_t>(tl - 1) & 1u, abort_flag,
+                                                 p.status, kWhereTileQueue, 0x20000000u | static_cast<unsigned>(tl),
+                                                 p.wait_ns))
+                    break;
+                Tile t;
+                if (!publish_tile<CG>(c, p, src, tl, atomicAdd(p.ticket, 1u), t, abort_flag, 0u)) break;
+                if (t.kind < 0) break;
+            }
         }
     } else if (FC && warp >= kThreads / 32) {
         // ------------------------------------------------------------ combine consumers
@@ -889,19 +1080,23 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         const bool publisher = (warp == 2 && lane == 0);
-        Scheduler sch(c, p);
         unsigned long long w_full = 0, w_work = 0, w_stores = 0, n1 = 0, n2 = 0;
         const unsigned long long t0 = tr ? clock64() : 0;
         if (tr && publisher) p.trace[blockIdx.x * kTraceWords + 12] = globaltimer_ns();
         for (int tl = 0;; ++tl) {
-            const Tile t = sch.next(c, E);
-            if (t.kind < 0) break;
+            Tile t;
+            // every lane waits for the descriptor; once all have read it, lane 0
+            // gives the slot back
+            const bool got = take_tile(c, p, tl, t, abort_flag);
+            __syncwarp();
+            if (lane == 0 && got) release_tile<CG>(c, tl, rank);
             const int b = tl & 1;
             const uint32_t aph = static_cast<uint32_t>(tl >> 1) & 1u;
             unsigned long long tw = tr ? clock64() : 0;
             // the whole warp agrees before its warp-collective tensor-memory loads
-            const bool ready = mbar_wait(&c.tfull[b], aph, abort_flag, p.status, kWhereEpiTmemFull,
-                                         static_cast<unsigned>(tl), p.wait_ns);
+            const bool ready = got && (t.kind < 0 || mbar_wait(&c.tfull[b], aph, abort_flag, p.status,
+                                                               kWhereEpiTmemFull, static_cast<unsigned>(tl),
+                                                               p.wait_ns));
             bool go = __all_sync(0xffffffffu, ready);
             if constexpr (TN) {
                 // warp pairs meet at named barriers below, so all four epilogue
@@ -912,6 +1107,7 @@ grouped_swiglu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                 go = *reinterpret_cast<volatile int *>(&c.epi_fail) == 0;
             }
             if (!go) break;
+            if (t.kind < 0) break;  // every warp read the same end marker
             unsigned long long *rec =
                 (publisher && p.tile_trace && tl < p.tile_trace_cap)
                     ? p.tile_trace + (static_cast<long>(blockIdx.x) * p.tile_trace_cap + tl) * kTileTraceWords
@@ -1267,9 +1463,9 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
     p.lead = a.lead > 0 ? a.lead : 2 * (p.group + (instances + p.P1 - 1) / p.P1) + 1;
     if (p.lead < p.group) p.lead = p.group;
     if (p.ring) {
-        // a ring of Q rows bounds the lead: Q >= D + group + 1
-        if (p.ring < 2 * p.group + 1 || p.schedule != 0) return cudaErrorInvalidConfiguration;
-        if (p.lead > p.ring - p.group - 1) p.lead = p.ring - p.group - 1;
+        // a ring of Q rows bounds the lead: Q >= D + 2 * group (see TileSource)
+        if (p.ring < 3 * p.group || p.schedule != 0) return cudaErrorInvalidConfiguration;
+        if (p.lead > p.ring - 2 * p.group) p.lead = p.ring - 2 * p.group;
     }
 
     const long R = a.R;
@@ -1286,8 +1482,8 @@ cudaError_t launch_cg(const FfnArgs &a, GemmParams p, cudaStream_t stream)
         return cudaErrorInvalidValue;
 
     if (!a.counters_zeroed) {
-        // l1_done and, right after it, l2_done
-        cudaError_t err = cudaMemsetAsync(a.l1_done, 0, 2 * sizeof(unsigned) * a.max_rows, stream);
+        // l1_done, l2_done right after it, then the tile ticket
+        cudaError_t err = cudaMemsetAsync(a.l1_done, 0, sizeof(unsigned) * (2 * a.max_rows + 1), stream);
         if (err != cudaSuccess) return err;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(instances * CG), 1, 1);
@@ -1306,6 +1502,7 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t stream)
     p.y = a.y;
     p.l1_done = a.l1_done;
     p.l2_done = a.l1_done + a.max_rows;
+    p.ticket = a.l1_done + 2 * a.max_rows;
     p.ring = a.h_ring_rows;
     // mixed row order: asked for (or by default) with the interleaved schedule;
     // not with the fused combine, whose consumers walk rows in expert order

@@ -98,7 +98,8 @@ Layout make_layout(const moe_shape_t *s, const moe_tuning_t *t = nullptr)
     L.bytes[MOE_WS_H] = ring ? ring * 256 * F * 2 : R * F * 2;
     L.bytes[MOE_WS_Y_PERM] = R * d * 2;
     L.bytes[MOE_WS_CHUNK_BASE] = chunks * E * 4;
-    L.bytes[MOE_WS_L1_DONE] = static_cast<size_t>(L.max_rows) * 8;  // Linear-1 then Linear-2 counts
+    // Linear-1 then Linear-2 counts, then the grouped GEMM's tile ticket
+    L.bytes[MOE_WS_L1_DONE] = (2 * static_cast<size_t>(L.max_rows) + 4) * 4;
     L.bytes[MOE_WS_L2_FLAGS] = static_cast<size_t>(L.max_rows) * p2max * 4;
     // h last: the other regions keep their offsets whatever h's size
     size_t off = 0;
@@ -423,7 +424,7 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     da.chunk_base = region<int32_t>(ws, L, MOE_WS_CHUNK_BASE);
     da.status = region<unsigned>(ws, L, MOE_WS_STATUS);
     da.zero_words = region<unsigned>(ws, L, MOE_WS_L1_DONE);
-    da.zero_count = 2 * L.max_rows;  // Linear-1 and Linear-2 row counters
+    da.zero_count = 2 * L.max_rows + 1;  // Linear-1 and Linear-2 row counters, tile ticket
     da.T = shape->T;
     da.d = shape->d;
     da.E = shape->E;

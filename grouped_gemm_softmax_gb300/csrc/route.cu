@@ -357,6 +357,171 @@ __global__ void __launch_bounds__(32 * WE * WT) route_kernel_async(const RoutePa
     select_topk<BE, NW>(p, lg, t0, BT, warp, lane);
 }
 
+// Large expert counts (E > 128), where the router is bound by the fp32 FMA
+// rate. Same thread layout and accumulation as route_kernel, but the staging
+// holds no registers: each chunk of kBK features is copied raw (bf16, 16-byte
+// cp.async, zero-filled past the end) into a shared-memory buffer while the
+// previous chunk is in use, then all threads widen it into the fp32 tiles in
+// one pass. The registers this frees let three blocks share an SM for the
+// smaller token tiles, and the FMAs of a 4-feature step run feature by
+// feature over the whole TM x TN tile, so consecutive FMAs never depend on
+// each other.
+template <int TM, int TN, int WE, int WT, int kBK>
+__global__ void __launch_bounds__(32 * WE * WT, TM <= 6 ? 3 : 2) route_kernel_cvt(const RouteParams p)
+{
+    constexpr int NT = 32 * WE * WT;
+    constexpr int BT = WT * 8 * TM;  // tokens per block
+    constexpr int BE = WE * 4 * TN;  // experts per block (>= E)
+    constexpr int NW = NT / 32;
+    constexpr int LD = kBK + 4;      // padded fp32 row (floats)
+    constexpr int RLD = kBK + 8;     // padded raw row (bf16): 16-byte aligned rows
+    constexpr int CPR = kBK / 8;     // 16-byte pieces per row
+    constexpr int ROWS = BT + BE;
+    extern __shared__ __align__(16) float rsm[];
+    float *xs = rsm;                                                // [BT][LD]
+    float *ws = rsm + BT * LD;                                      // [BE][LD]
+    uint16_t *raw = reinterpret_cast<uint16_t *>(rsm + ROWS * LD);  // [ROWS][RLD]
+    float *lg = rsm;                                                // [BT][BE + 1] after the K loop
+    pdl_wait();
+    pdl_trigger();
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int a = lane & 7, b = lane >> 3;
+    const int eb = (warp % WE) * 4 * TN, tb = (warp / WE) * 8 * TM;
+    const long t0 = static_cast<long>(blockIdx.x) * BT;
+    const int nchunks = (p.d + kBK - 1) / kBK;
+
+    auto issue = [&](int chunk) {
+        const int k0 = chunk * kBK;
+        for (int v = tid; v < ROWS * CPR; v += NT) {
+            const int r = v / CPR, c8 = (v % CPR) * 8;
+            const bool is_x = r < BT;
+            const long row = is_x ? t0 + r : static_cast<long>(r - BT);
+            const bool ok = k0 + c8 < p.d && (is_x ? row < p.T : row < p.E);
+            const uint16_t *src = is_x ? p.x + (ok ? row * p.d + k0 + c8 : 0)
+                                       : p.wr + (ok ? row * p.d + k0 + c8 : 0);
+            cp_async_16(raw + r * RLD + c8, src, ok);
+        }
+    };
+    auto widen_chunk = [&]() {
+        const uint16_t *st = raw;
+        for (int v = tid; v < ROWS * CPR; v += NT) {
+            const int r = v / CPR, c8 = (v % CPR) * 8;
+            const uint4 q = *reinterpret_cast<const uint4 *>(st + r * RLD + c8);
+            float *dst = r < BT ? xs + r * LD + c8 : ws + (r - BT) * LD + c8;
+            *reinterpret_cast<float4 *>(dst) =
+                make_float4(bf16_bits_to_f32(q.x & 0xFFFFu), bf16_bits_to_f32(q.x >> 16),
+                            bf16_bits_to_f32(q.y & 0xFFFFu), bf16_bits_to_f32(q.y >> 16));
+            *reinterpret_cast<float4 *>(dst + 4) =
+                make_float4(bf16_bits_to_f32(q.z & 0xFFFFu), bf16_bits_to_f32(q.z >> 16),
+                            bf16_bits_to_f32(q.w & 0xFFFFu), bf16_bits_to_f32(q.w >> 16));
+        }
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+    issue(0);
+    cp_async_commit();
+    for (int c = 0; c < nchunks; ++c) {
+        cp_async_wait<0>();  // chunk c has landed (the only copies in flight)
+        __syncthreads();     // ... for every thread, and chunk c - 1's tiles are no longer read
+        widen_chunk();
+        __syncthreads();     // tiles of chunk c ready; the raw buffer is free again
+        if (c + 1 < nchunks) issue(c + 1);  // lands while chunk c is used
+        cp_async_commit();
+#pragma unroll 2
+        for (int kk = 0; kk < kBK; kk += 4) {
+            float4 xv[TM], wv[TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+                xv[i] = *reinterpret_cast<const float4 *>(xs + (tb + a + 8 * i) * LD + kk);
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                wv[j] = *reinterpret_cast<const float4 *>(ws + (eb + b + 4 * j) * LD + kk);
+            // ascending feature order for every (token, expert) accumulator
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].x, wv[j].x, acc[i][j]);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].y, wv[j].y, acc[i][j]);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].z, wv[j].z, acc[i][j]);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].w, wv[j].w, acc[i][j]);
+        }
+    }
+    __syncthreads();  // every thread is done with the tiles before the logits overwrite them
+
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int e = eb + b + 4 * j;
+            float z = acc[i][j];
+            if (p.bias != nullptr && e < p.E) z = z + p.bias[e];
+            lg[(tb + a + 8 * i) * (BE + 1) + e] = z;
+        }
+    }
+    __syncthreads();
+    select_topk<BE, NW>(p, lg, t0, BT, warp, lane);
+}
+
+template <int TM, int TN, int WE, int WT, int kBK>
+struct CvtVariant {
+    static constexpr int NT = 32 * WE * WT;
+    static constexpr int BT = WT * 8 * TM;
+    static constexpr int BE = WE * 4 * TN;
+    static constexpr size_t tiles =
+        sizeof(float) * (kBK + 4) * (BT + BE) + sizeof(uint16_t) * (BT + BE) * (kBK + 8);
+    static constexpr size_t logits = sizeof(float) * BT * (BE + 1);
+    static constexpr size_t smem = tiles > logits ? tiles : logits;
+
+    // once per device: the shared-memory attribute, and how many blocks fit
+    // on an SM (registers and shared memory); 0 when the setup failed
+    static int blocks_per_sm()
+    {
+        struct Tag {};
+        static int occ[kOnceDevices];
+        const cudaError_t e = once_per_device<Tag>([](int dev) {
+            cudaError_t err = cudaFuncSetAttribute(route_kernel_cvt<TM, TN, WE, WT, kBK>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+            if (err != cudaSuccess) return err;
+            int n = 0;
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_kernel_cvt<TM, TN, WE, WT, kBK>, NT,
+                                                                smem);
+            if (err == cudaSuccess && dev >= 0 && dev < kOnceDevices) occ[dev] = n;
+            return err;
+        });
+        if (e != cudaSuccess) return 0;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kOnceDevices) return 1;
+        return occ[dev];
+    }
+
+    static cudaError_t launch(const RouteParams &p, cudaStream_t s)
+    {
+        if (blocks_per_sm() <= 0) {
+            const cudaError_t e = cudaGetLastError();
+            return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+        }
+        const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
+        return launch_pdl(route_kernel_cvt<TM, TN, WE, WT, kBK>, dim3(grid), dim3(NT), smem, s, p);
+    }
+};
+
 template <int TM, int TN, int WE, int WT, int kBK>
 cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
 {
@@ -404,18 +569,20 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     // a block covers every expert (BE = 4*WE*TN >= E) and BT = 8*WT*TM tokens
     // <TM, TN, WE, WT, chunk>: measured best per expert count on GB300
     if (a.E > 128) {
-        // BE 256 as 4 warps x 4 expert lanes x 16 experts per thread, 128
-        // threads and <= 255 registers, so two blocks share an SM. The token
-        // tile (8 * TM tokens) is the one whose last wave of blocks is
-        // fullest, slightly favouring larger tiles (more reuse of each staged
-        // feature chunk). fine (T = 16384, 152 SMs): TM = 7 gives 293 blocks,
-        // one wave of 304 slots, 801 us; the same tile with 8 experts per
-        // thread and 8 warps (one block per SM, two waves) took 828 us.
+        // BE 256 as 4 warps x 4 expert lanes x 16 experts per thread (128
+        // threads), TM tokens per thread. The token tile (8 * TM tokens) is
+        // the one whose last wave of blocks is fullest, counting the blocks
+        // that fit on an SM for each tile (TM <= 6 needs ~170 registers, so
+        // three blocks fit; TM 7-8 take up to 255, two blocks), slightly
+        // favouring larger tiles (more reuse of each staged feature chunk).
         const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
-        const long slots = 2L * sms;
+        const int occ[5] = {CvtVariant<4, 16, 4, 1, 32>::blocks_per_sm(), CvtVariant<5, 16, 4, 1, 32>::blocks_per_sm(),
+                            CvtVariant<6, 16, 4, 1, 32>::blocks_per_sm(), CvtVariant<7, 16, 4, 1, 32>::blocks_per_sm(),
+                            CvtVariant<8, 16, 4, 1, 32>::blocks_per_sm()};
         int best_tm = 8;
         double best = -1.0;
         for (int tm = 8; tm >= 4; --tm) {
+            const long slots = static_cast<long>(occ[tm - 4] > 0 ? occ[tm - 4] : 1) * sms;
             const long blocks = (a.T + 8L * tm - 1) / (8L * tm);
             const long waves = (blocks + slots - 1) / slots;
             const double score = static_cast<double>(blocks) / (waves * slots) * (1.0 - 0.02 * (8 - tm));
@@ -425,11 +592,11 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
             }
         }
         switch (best_tm) {
-        case 7: return launch_variant<7, 16, 4, 1, 32>(p, s);
-        case 6: return launch_variant<6, 16, 4, 1, 32>(p, s);
-        case 5: return launch_variant<5, 16, 4, 1, 32>(p, s);
-        case 4: return launch_variant<4, 16, 4, 1, 32>(p, s);
-        default: return launch_variant<8, 16, 4, 1, 32>(p, s);
+        case 7: return CvtVariant<7, 16, 4, 1, 32>::launch(p, s);
+        case 6: return CvtVariant<6, 16, 4, 1, 32>::launch(p, s);
+        case 5: return CvtVariant<5, 16, 4, 1, 32>::launch(p, s);
+        case 4: return CvtVariant<4, 16, 4, 1, 32>::launch(p, s);
+        default: return CvtVariant<8, 16, 4, 1, 32>::launch(p, s);
         }
     }
     if (a.E > 64) return launch_variant<2, 8, 4, 2, 64>(p, s);    // BT 32, BE 128

@@ -18,7 +18,7 @@ enum : unsigned { kStatusBadExpert = 1u, kStatusBadOffsets = 1u, kStatusTimeout 
 enum : unsigned {
     kWhereProducerEmpty = 1, kWhereProducerDep = 2, kWhereMmaFull = 3, kWhereMmaTmemEmpty = 4,
     kWhereEpiTmemFull = 5, kWhereDispatch = 6, kWhereGemmOffsets = 7, kWhereCombine = 8,
-    kWhereMmaDrain = 9, kWhereLoadDrain = 10
+    kWhereMmaDrain = 9, kWhereLoadDrain = 10, kWhereTileQueue = 11
 };
 
 // Default wall-clock limit of any single wait (ns). The longest legitimate
@@ -130,6 +130,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// mbar_wait for a barrier that threads of another CTA of the cluster arrive
+// on, with cluster-scope acquire (their writes before the arrival are visible
+// after it).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *cta_abort,
+                                                  unsigned *status, unsigned where, unsigned detail,
+                                                  unsigned long long limit_ns)
+{
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(a, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (*cta_abort) return false;
+            if (ld_volatile_u32(status) != 0u) {
+                *cta_abort = 1;
+                return false;
+            }
+            if (globaltimer_ns() - t0 > limit_ns) {
+                report_failure(status, kStatusTimeout, where, detail);
+                *cta_abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait that ignores abort requests (used to drain outstanding work
 // before tensor memory is freed). Returns false if the limit ran out.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
@@ -224,6 +264,14 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
     return v;
+}
+
+// 16-byte store to a shared::cluster address (another CTA's shared memory)
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, int4 v)
+{
+    asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 // arrive on an mbarrier that may live in another CTA of the cluster

@@ -88,7 +88,7 @@ typedef enum {
 typedef struct {
     int schedule;   /* moe_schedule_t */
     int lead_rows;  /* D: minimum lead of Linear-1 over Linear-2 in scheduler rows; 0 = default;
-                       raised to group_rows if smaller (needed for deadlock freedom) */
+                       raised to the raster group if smaller (needed for deadlock freedom) */
     int num_ctas;   /* persistent grid size in CTAs (rounded down to whole CTA groups); 0 = as
                        many as are co-resident (one per SM) */
     int l2_block_n; /* Linear-2 tile width (64, 128, 192 or 256) with tokens on the M side;
@@ -116,11 +116,12 @@ typedef struct {
                            (Xian et al., Algorithm 1, "destination ring slot"): row p lives in
                            slot p mod Q and a Linear-1 tile of row p >= Q waits (bounded)
                            until every Linear-2 tile of row p - Q has finished. Q must be at
-                           least 2 * raster group + 1 scheduler rows (33 with the defaults)
-                           and the lead is lowered to Q - group - 1 if above it, which keeps
-                           the waits deadlock-free; interleaved schedule only (else
-                           MOE_ERR_INVALID_ARG). The workspace must then come from
-                           moe_workspace_bytes_tuned with the same tuning. */
+                           least 3 * raster group scheduler rows (48 for CTA pairs with the
+                           default group of 32 M-tiles, 24 with 16) and the lead is lowered
+                           to Q - 2 * group if above it, which keeps the waits deadlock-free;
+                           interleaved schedule only (else MOE_ERR_INVALID_ARG). The
+                           workspace must then come from moe_workspace_bytes_tuned with the
+                           same tuning. */
     int fused_combine;  /* moe_layer_forward_tuned / _ex only (else MOE_ERR_INVALID_ARG): 1 =
                            combine inside the grouped GEMM (Cui et al. section 3.3: consumers
                            poll the per-row Linear-2 completion and write each token to its
@@ -164,7 +165,8 @@ enum {
     MOE_WS_Y_PERM = 9,      /* [R,d] bf16 */
     MOE_WS_CHUNK_BASE = 10, /* dispatch scratch: [chunks,E] int32 */
     MOE_WS_L1_DONE = 11,    /* per scheduler row: finished Linear-1 tiles, u32; then per row the
-                               finished Linear-2 tiles (used by the h ring) */
+                               finished Linear-2 tiles (used by the h ring); then the grouped
+                               GEMM's tile ticket counter */
     MOE_WS_L2_FLAGS = 12,   /* per Linear-2 tile: ready flag = epoch of the call that wrote it, u32
                                (a call captured in a CUDA Graph keeps its capture-time epoch on
                                every replay) */

@@ -17,9 +17,9 @@ pytestmark = pytest.mark.gpu
 
 # where the timeout is recorded: the producer's wait for the Linear-1 rows, or
 # a wait that starves behind it (the MMA thread's wait for the next loaded
-# stage, the epilogue's wait for the next accumulator), whichever limit runs
-# out first
-WHERE_STARVED = {2, 3, 5}
+# stage, the epilogue's wait for the next accumulator, a wait on the CTA's
+# tile-descriptor queue), whichever limit runs out first
+WHERE_STARVED = {2, 3, 5, 11}
 
 
 def _case(counts, d, F):

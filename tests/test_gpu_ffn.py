@@ -158,7 +158,7 @@ def test_h_ring_is_bit_identical_to_full_h(mode):
     base = dict(MODES[mode], group_rows=4)
     _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(**base))
     group = 4 // MODES[mode]["cta_group"]  # raster group in scheduler rows
-    for ring, order in ((2 * group + 1, 0), (12, 0), (2 * group + 1, 2)):
+    for ring, order in ((3 * group, 0), (13, 0), (3 * group, 2)):
         t = moe.Tuning(**base, h_ring_rows=ring, row_order=order)
         s = moe.Shape(T=c["R"], d=c["d"], E=c["E"], top_k=1, ffn=c["F"])
         ws = moe.alloc_workspace(s, tuning=t)
@@ -171,7 +171,7 @@ def test_h_ring_below_the_deadlock_free_size_is_refused():
     need_gpu()
     c = make_case([300, 200], 256, 256, seed=14)
     s = moe.Shape(T=c["R"], d=c["d"], E=c["E"], top_k=1, ffn=c["F"])
-    t = moe.Tuning(h_ring_rows=8)  # default raster group: 16 pair rows -> needs >= 33
+    t = moe.Tuning(h_ring_rows=8)  # default raster group here: 8 pair rows -> needs >= 24
     ws = moe.alloc_workspace(s, tuning=t)
     y = torch.zeros(c["R"], c["d"], dtype=torch.bfloat16, device="cuda")
     off = torch.from_numpy(c["offsets"]).cuda()

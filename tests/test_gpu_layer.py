@@ -193,7 +193,7 @@ def test_fused_combine_with_h_ring_and_a_timeout():
     cfg = custom_cfg(4096, 256, 8, 2, 256, S=2)
     layer = GpuLayer(cfg, seed=3)
     a = layer.forward().clone()
-    t = moe.Tuning(fused_combine=1, h_ring_rows=40)
+    t = moe.Tuning(fused_combine=1, h_ring_rows=48)
     ws = moe.alloc_workspace(layer.shape, tuning=t)
     i = layer.inp
     moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=t)
