@@ -269,7 +269,7 @@ def timeline_summary(moe, cfg, shape, inp, ws, tuning, dev):
     gaps between consecutive tiles and the Linear-2 producers' waits for
     Linear-1 rows."""
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    cap = int((((cfg.R + 127) // 128 + cfg.E) * ((cfg.F + cfg.d) // 64)) // sms) + 64
+    cap = moe.tile_trace_capacity(shape, sms)
     words = moe.TILE_TRACE_WORDS
     tt = torch.zeros(sms * cap * words, dtype=torch.int64, device=dev)
     tr = torch.zeros(sms * moe.TRACE_WORDS, dtype=torch.int64, device=dev)

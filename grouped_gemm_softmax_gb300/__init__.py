@@ -219,6 +219,14 @@ def alloc_workspace(shape: Shape, device="cuda", tuning: Tuning | None = None) -
     return ws
 
 
+def tile_trace_capacity(shape: Shape, num_ctas: int) -> int:
+    """Per-CTA record count for Tuning.tile_trace that holds every tile a CTA can
+    run: the tiles of the smallest (128-row) scheduler rows spread over the
+    CTAs, plus 64 for the uneven spread of dynamically claimed tiles."""
+    rows = (shape.T * shape.top_k + 127) // 128 + shape.E
+    return rows * ((shape.ffn + shape.d) // 64) // max(num_ctas, 1) + 64
+
+
 def ws_view(ws: torch.Tensor, shape: Shape, region: int, dtype, dims) -> torch.Tensor:
     """A typed view of one workspace region (no copy)."""
     off, nb = workspace_region(shape, region)

@@ -86,10 +86,10 @@ class GpuLayer:
         )
 
 
-def oracle_route(layer: GpuLayer):
+def oracle_route(layer: GpuLayer, keep_logits: bool = False):
     i, cfg = layer.inp, layer.cfg
     bias = None if i.bias is None else i.bias.cpu().numpy()
-    return oracle.route(bits(i.x), bits(i.wr), bias, cfg.k)
+    return oracle.route(bits(i.x), bits(i.wr), bias, cfg.k, keep_logits=keep_logits)
 
 
 def check_route(idx_gpu, gate_gpu, ref):
@@ -118,11 +118,14 @@ def sample_tokens(T, n, seed=0):
 def compact_experts(layer: GpuLayer, experts):
     """Weights of only the listed experts (host bf16 bits) and the expert -> slot map."""
     experts = sorted(set(int(e) for e in experts))
-    sel = torch.tensor(experts, dtype=torch.long, device=layer.inp.w1.device)
     i = layer.inp
-    w1 = bits(i.w1.index_select(0, sel))
-    w3 = bits(i.w3.index_select(0, sel))
-    w2 = bits(i.w2.index_select(0, sel))
+    if len(experts) == layer.cfg.E:  # all of them: no device-side copy
+        w1, w3, w2 = bits(i.w1), bits(i.w3), bits(i.w2)
+    else:
+        sel = torch.tensor(experts, dtype=torch.long, device=layer.inp.w1.device)
+        w1 = bits(i.w1.index_select(0, sel))
+        w3 = bits(i.w3.index_select(0, sel))
+        w2 = bits(i.w2.index_select(0, sel))
     remap = np.full(layer.cfg.E, -1, np.int32)
     remap[experts] = np.arange(len(experts), dtype=np.int32)
     return w1, w3, w2, remap

@@ -157,6 +157,10 @@ def test_h_ring_is_bit_identical_to_full_h(mode):
     c = make_case([70, 0, 129, 1, 255, 57, 300, 12] * 8, 256, 384, seed=13)
     base = dict(MODES[mode], group_rows=4)
     _, _, h0, y0 = run_ffn(c, tuning=moe.Tuning(**base))
+    # the reference output itself against the oracle (every row)
+    href, yref = oracle_rows(c, np.arange(c["R"]))
+    assert_close(to_f64(h0), href, f"{mode} h")
+    assert_close(to_f64(y0), yref, f"{mode} y")
     group = 4 // MODES[mode]["cta_group"]  # raster group in scheduler rows
     for ring, order in ((3 * group, 0), (13, 0), (3 * group, 2)):
         t = moe.Tuning(**base, h_ring_rows=ring, row_order=order)

@@ -18,6 +18,7 @@ import synth
 from conftest import f32_to_bf16_bits
 from gpu_helpers import (GpuLayer, assert_close, bits, check_dispatch, check_route, compact_experts,
                          custom_cfg, need_gpu, oracle_route, sample_tokens, to_f64)
+from routing_checks import check_fp64_selection
 
 pytestmark = pytest.mark.gpu
 
@@ -48,11 +49,19 @@ def test_hand_example_on_gpu():
     np.testing.assert_array_equal(sor, g["slot_of_row"])
 
 
-def _full_compare(layer, out, n_tokens, n_rows, seed=0):
+def _full_compare(layer, out, n_tokens, n_rows, seed=0, every_band=False):
+    """Routing and dispatch bit-exact; y_perm on sampled rows and out on sampled
+    tokens within the tolerances. every_band: y_perm also on one row of every
+    128-row band of every expert (so every scheduler row of the grouped GEMM,
+    128 or 256 rows, in either operand orientation) and on each expert's last row;
+    and the fp64 selection check on the GPU's indices."""
     cfg = layer.cfg
-    ref = oracle_route(layer)
+    ref = oracle_route(layer, keep_logits=every_band)
     idx, gate = layer.routing()
     check_route(idx, gate, ref)
+    if every_band:
+        sens = check_fp64_selection(idx, bits(layer.inp.x), bits(layer.inp.wr), ref)
+        print(f"{cfg.name}: {len(sens)} fp-sensitive tokens {list(sens[:8])}")
     disp = check_dispatch(layer.dispatch_state(), ref.idx, cfg.E)
     # y_perm on sampled rows (first and last row of every expert among them)
     rows = set()
@@ -61,6 +70,13 @@ def _full_compare(layer, out, n_tokens, n_rows, seed=0):
         a, b = disp.offsets[e], disp.offsets[e + 1]
         if b > a:
             rows.update([a, b - 1, (a + b) // 2])
+    if every_band:
+        for e in range(cfg.E):
+            a, b = int(disp.offsets[e]), int(disp.offsets[e + 1])
+            for r0 in range(a, b, 128):
+                rows.add(int(rng.integers(r0, min(r0 + 128, b))))
+            if b > a:
+                rows.add(b - 1)
     rows.update(rng.choice(cfg.R, size=min(cfg.R, n_rows), replace=False).tolist())
     rows = np.array(sorted(rows), np.int64)
     er = np.searchsorted(disp.offsets, rows, side="right") - 1
@@ -159,7 +175,10 @@ def test_layer_with_h_ring_is_bit_identical():
     i = layer.inp
     moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=t)
     assert moe.last_device_status(ws) == moe.MOE_OK
-    assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), a.view(torch.int16))
+    ring_out = torch.cat(layer.out, 0)
+    assert torch.equal(ring_out.view(torch.int16), a.view(torch.int16))
+    layer.ws = ws  # the ring call's routing, permutation and y_perm, against the oracle
+    _full_compare(layer, ring_out, n_tokens=cfg.T, n_rows=cfg.R)
 
 
 FUSED_CASES = [custom_cfg(1000, 136, 5, 3, 200, S=8, zipf_s=2.0), custom_cfg(333, 256, 33, 4, 128, S=3, zipf_s=1.0),
@@ -183,6 +202,7 @@ def test_fused_combine_is_bit_identical(cfg, mode):
         seg.fill_(float("nan"))
     b = layer.forward(tuning=moe.Tuning(**GEMM_MODES[mode], fused_combine=1))
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _full_compare(layer, b, n_tokens=min(cfg.T, 512), n_rows=min(cfg.R, 256))
 
 
 def test_fused_combine_with_h_ring_and_a_timeout():
@@ -199,6 +219,9 @@ def test_fused_combine_with_h_ring_and_a_timeout():
     moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=t)
     assert moe.last_device_status(ws) == moe.MOE_OK
     assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), a.view(torch.int16))
+    ring_ws, layer.ws = layer.ws, ws
+    _full_compare(layer, torch.cat(layer.out, 0), n_tokens=512, n_rows=512)
+    layer.ws = ring_ws
     bad = moe.Tuning(fused_combine=1, wait_limit_us=20000, unmet_dependency=1)
     moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, ws, tuning=bad)
     assert moe.last_device_status(ws) == moe.MOE_ERR_TIMEOUT
@@ -220,7 +243,42 @@ def test_full_size_configs(name):
     for order in (1, 2):
         out4 = layer.forward(tuning=moe.Tuning(row_order=order))
         assert torch.equal(out.view(torch.int16), out4.view(torch.int16))
-    maxrel, fro = _full_compare(layer, out, n_tokens=24, n_rows=48)
+    maxrel, fro = _full_compare(layer, out, n_tokens=256, n_rows=48, every_band=True)
     print(f"{name}: max err / max|ref| = {maxrel:.2e}, rel Frobenius = {fro:.2e}")
     del layer
     torch.cuda.empty_cache()
+
+
+def test_tile_timeline_records_every_tile_once():
+    """The per-tile timeline (Xian et al., section 5.2.3: per-tile mainloop and
+    epilogue spans measured in the kernel) does not change the results, records
+    every tile of the layer exactly once in the CTA pair that ran it, with MMA
+    start <= last MMA issue <= end of the epilogue stores, and is not truncated
+    when sized as the bench sizes it."""
+    need_gpu()
+    cfg = custom_cfg(3000, 256, 8, 2, 512, zipf_s=1.0)  # tokens on the N side, CTA pairs
+    layer = GpuLayer(cfg, seed=4)
+    plain = layer.forward().clone()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cap = moe.tile_trace_capacity(layer.shape, sms)
+    tt = torch.zeros(sms * cap * moe.TILE_TRACE_WORDS, dtype=torch.int64, device="cuda")
+    tr = torch.zeros(sms * moe.TRACE_WORDS, dtype=torch.int64, device="cuda")
+    traced = layer.forward(tuning=moe.Tuning(trace=tr, tile_trace=tt, tile_trace_cap=cap))
+    assert torch.equal(plain.view(torch.int16), traced.view(torch.int16))
+    rec = tt.view(sms, cap, moe.TILE_TRACE_WORDS).cpu().numpy().astype(np.int64)
+    assert not (rec[:, -1, 1] > 0).any(), "timeline truncated"
+    # the tiles of the layer: 256-token scheduler rows, Linear-1 tiles of 128 h
+    # columns and Linear-2 tiles of 256 y columns per row
+    counts = np.diff(layer.dispatch_state()["offsets"])
+    P = int(sum((int(c) + 255) // 256 for c in counts))
+    P1, P2 = (cfg.F + 127) // 128, (cfg.d + 255) // 256
+    expected = sorted([(0, r, n) for r in range(P) for n in range(P1)] +
+                      [(1, r, n) for r in range(P) for n in range(P2)])
+    got = []
+    for cta in range(0, sms, 2):  # the first CTA of each pair issues the MMAs
+        for w in rec[cta]:
+            if w[3] == 0:
+                continue
+            got.append((int(w[0] & 3), int((w[0] >> 2) & 0xFFFFFFFF), int(w[0] >> 34)))
+            assert w[1] > 0 and w[3] <= w[4] <= w[7], w
+    assert sorted(got) == expected
