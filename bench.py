@@ -43,7 +43,6 @@ import synth  # noqa: E402
 METRIC = "MoE-layer tokens/s and TFLOP/s on 1 GB300; fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 7  # route, count, scan, rank, copy, grouped GEMM, combine
 
 
 def parse_args():
@@ -76,7 +75,19 @@ def parse_args():
                          "per-tile timeline summary to the line")
     ap.add_argument("--stage", choices=["route", "dispatch", "combine"], default=None,
                     help="time one entry point alone (for profiling) instead of the layer")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling: the workload cut down to this many experts, with T scaled so the "
+                         "tokens per expert (and d, ffn, top_k) stay the same")
     return ap.parse_args()
+
+
+def scaled_config(cfg, experts):
+    """The workload with fewer experts and proportionally fewer tokens: same d,
+    ffn, top_k, routing skew and tokens per expert (T a multiple of the segments)."""
+    if experts <= 0 or experts >= cfg.E:
+        return cfg
+    T = max(cfg.S, cfg.T * experts // cfg.E // cfg.S * cfg.S)
+    return dataclasses.replace(cfg, name=f"{cfg.name}-{experts}e", T=T, E=experts)
 
 
 def load_peaks():
@@ -262,8 +273,8 @@ def traffic_record(cfg_name):
 
 
 def timeline_summary(moe, cfg, shape, inp, ws, tuning, dev):
-    """One extra grouped-GEMM launch, outside the timed region, with the per-tile
-    timeline switched on. Cycle counts are each SM's own clock64; only
+    """One extra layer call, outside the timed region, with the grouped GEMM's
+    per-tile timeline switched on. Cycle counts are each SM's own clock64; only
     per-CTA differences are used. Summarises how much of each MMA issuer's
     span went to issuing tiles, the stage (operand) waits inside tiles, the
     gaps between consecutive tiles and the Linear-2 producers' waits for
@@ -273,11 +284,9 @@ def timeline_summary(moe, cfg, shape, inp, ws, tuning, dev):
     words = moe.TILE_TRACE_WORDS
     tt = torch.zeros(sms * cap * words, dtype=torch.int64, device=dev)
     tr = torch.zeros(sms * moe.TRACE_WORDS, dtype=torch.int64, device=dev)
-    xp = moe.ws_view(ws, shape, moe.WS.X_PERM, torch.bfloat16, (cfg.R, cfg.d))
-    off = moe.ws_view(ws, shape, moe.WS.OFFSETS, torch.int32, (cfg.E + 1,))
-    y = moe.ws_view(ws, shape, moe.WS.Y_PERM, torch.bfloat16, (cfg.R, cfg.d))
+    out = [torch.empty(cfg.T // cfg.S, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
     traced = dataclasses.replace(tuning, trace=tr, tile_trace=tt, tile_trace_cap=cap)
-    moe.expert_ffn(shape, xp, off, inp.w1, inp.w3, inp.w2, y, ws, tuning=traced)
+    moe.layer_forward(shape, inp.x, inp.wr, inp.bias, inp.w1, inp.w3, inp.w2, out, ws, tuning=traced)
     torch.cuda.synchronize(dev)
     st = moe.last_device_status(ws)
     if st != moe.MOE_OK:
@@ -547,7 +556,7 @@ def run_ours(args, cfg):
         "stage_ms": {"route": float(stage_ms[:, 0].mean()), "dispatch": float(stage_ms[:, 1].mean()),
                      "grouped_gemm": gemm_ms, "combine": float(stage_ms[:, 3].mean())},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "graph": graph,
-        "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks,
+        "gpu_launches": moe.layer_kernel_launches(shape, tuning) * args.steps, "clocks": clocks,
         "wall_s_timed": t_wall,
     }
     if args.lead:
@@ -562,7 +571,6 @@ def run_ours(args, cfg):
         line["config"]["row_order"] = args.row_order
     if args.fused_combine:
         line["config"]["fused_combine"] = True
-        line["gpu_launches"] = (KERNELS_PER_STEP - 1) * args.steps
     if args.h_ring:
         line["config"]["h_ring_rows"] = args.h_ring
         line["workspace_bytes"] = int(ws.numel())
@@ -640,7 +648,7 @@ def run_stage(args, cfg):
 
 def main():
     args = parse_args()
-    cfg = synth.CONFIGS[args.config]
+    cfg = scaled_config(synth.CONFIGS[args.config], args.experts)
     if args.stage:
         run_stage(args, cfg)
     elif args.impl == "reference":

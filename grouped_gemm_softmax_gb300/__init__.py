@@ -142,6 +142,7 @@ def library():
             "moe_layer_forward": ([S, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "moe_layer_forward_tuned": ([S, TU, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "moe_layer_forward_ex": ([S, TU, P, P, P, P, P, P, P, P, sz, P, P], ctypes.c_int),
+            "moe_layer_kernel_launches": ([S, TU], ctypes.c_int),
             "moe_last_device_status": ([P, P], ctypes.c_int),
             "moe_last_device_detail": ([ctypes.POINTER(ctypes.c_uint32)] * 3, None),
         }
@@ -217,6 +218,12 @@ def alloc_workspace(shape: Shape, device="cuda", tuning: Tuning | None = None) -
     ws = torch.empty(nb, dtype=torch.uint8, device=device)
     ws[:16].zero_()  # device status word
     return ws
+
+
+def layer_kernel_launches(shape: Shape, tuning: Tuning | None = None) -> int:
+    """How many kernels one layer_forward call launches for this shape and tuning."""
+    t = ctypes.byref(tuning.c()) if tuning is not None else None
+    return int(library().moe_layer_kernel_launches(ctypes.byref(shape.c()), t))
 
 
 def tile_trace_capacity(shape: Shape, num_ctas: int) -> int:

@@ -455,6 +455,14 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     return MOE_OK;
 }
 
+int moe_layer_kernel_launches(const moe_shape_t *shape, const moe_tuning_t *tuning)
+{
+    if (check_shape(shape) != MOE_OK || check_tuning(tuning) != MOE_OK) return 0;
+    const bool fused = tuning && tuning->fused_combine;
+    // route; count, scan, rank, copy; grouped GEMM; combine
+    return 1 + 4 + 1 + (fused ? 0 : 1);
+}
+
 moe_status_t moe_layer_forward_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,
                                      const moe_bf16_t *x, const moe_bf16_t *w_router,
                                      const float *expert_bias, const moe_bf16_t *W1,

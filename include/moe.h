@@ -279,6 +279,12 @@ moe_status_t moe_layer_forward(const moe_shape_t *shape, const moe_bf16_t *x,
                                moe_bf16_t *const *out_segments, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* Kernel launches one moe_layer_forward_tuned call makes for this shape and
+ * tuning (NULL = defaults): route, the dispatch's count, scan, rank and row
+ * copy, the grouped GEMM, and the combine unless fused_combine. 0 for an
+ * invalid shape or tuning; the layer makes no launch at all when T == 0. */
+int moe_layer_kernel_launches(const moe_shape_t *shape, const moe_tuning_t *tuning);
+
 /* moe_layer_forward with an explicit tile schedule (tuning may be NULL); the
  * workspace is sized by moe_workspace_bytes_tuned(shape, tuning). */
 moe_status_t moe_layer_forward_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,

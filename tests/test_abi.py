@@ -197,3 +197,14 @@ def test_row_order_values_are_checked(lib):
         assert lib.moe_expert_ffn_tuned(c, ctypes.byref(bad.c()), fake, fake, fake, fake, fake, fake,
                                         fake, nb, None) == moe.MOE_ERR_INVALID_ARG
 
+
+
+def test_layer_kernel_launches(lib):
+    """Host-side count of the layer's launches: route, four dispatch kernels,
+    the grouped GEMM and the combine (none when the combine is fused into the
+    GEMM)."""
+    fine = moe.Shape(T=16384, d=4096, E=256, top_k=8, ffn=2048)
+    assert moe.layer_kernel_launches(fine) == 7
+    assert moe.layer_kernel_launches(fine, moe.Tuning(fused_combine=1)) == 6
+    bad = moe.Shape(T=10, d=12, E=4, top_k=2, ffn=16)  # d not a multiple of 8
+    assert moe.layer_kernel_launches(bad) == 0
