@@ -239,13 +239,11 @@ moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const moe_bf16_t *x,
  * off[E]=R; other offsets are recorded as MOE_ERR_INVALID_ARG in the device
  * status and nothing is computed); W1, W3 [E,F,d] bf16; W2 [E,d,F] bf16;
  * y_perm [R,d] bf16 (out); h lives in the workspace (region MOE_WS_H).
- * The grouped GEMM is a persistent grid of one CTA (or CTA pair) per SM whose
- * Linear-2 tiles wait for Linear-1 tiles of other CTAs, so it needs its whole
- * grid resident at once: do not run two grouped GEMMs (moe_expert_ffn or a
- * layer call, any stream, any thread) on one device at the same time. Two
- * such grids that each got only part of the SMs would wait on each other
- * until the bounded waits run out (MOE_ERR_TIMEOUT, outputs incomplete).
- * Other kernels running beside it only delay it. */
+ * The grouped GEMM is a persistent grid of one CTA (or CTA pair) per SM. Its
+ * CTAs take tiles in one global order from a counter in the workspace, and a
+ * tile only ever waits for tiles earlier in that order, which running CTAs
+ * hold; so it completes whatever share of the GPU it gets, also beside other
+ * grouped GEMMs (other streams, other threads, other workspaces). */
 moe_status_t moe_expert_ffn(const moe_shape_t *shape, const moe_bf16_t *x_perm,
                             const int32_t *expert_offsets, const moe_bf16_t *W1,
                             const moe_bf16_t *W3, const moe_bf16_t *W2, moe_bf16_t *y_perm,
@@ -271,8 +269,7 @@ moe_status_t moe_combine(const moe_shape_t *shape, const moe_bf16_t *y_perm,
 /* The whole layer: route -> dispatch -> grouped SwiGLU GEMM -> combine, seven
  * kernel launches on one stream (route; count, scan, rank and copy for the
  * dispatch; the grouped GEMM; combine), no host synchronisation. Intermediates
- * (routing, permutation, x_perm, h, y_perm) stay in the workspace regions.
- * The same rule on concurrent grouped GEMMs as moe_expert_ffn applies. */
+ * (routing, permutation, x_perm, h, y_perm) stay in the workspace regions. */
 moe_status_t moe_layer_forward(const moe_shape_t *shape, const moe_bf16_t *x,
                                const moe_bf16_t *w_router, const float *expert_bias,
                                const moe_bf16_t *W1, const moe_bf16_t *W3, const moe_bf16_t *W2,

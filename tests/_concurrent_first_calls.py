@@ -1,12 +1,10 @@
 """Run as a fresh process by test_gpu_layer.py: several threads make the very
-first layer calls of the process at the same time, each with its own inputs
-and workspace, so the library's one-time per-device launch setup races; every
-result must equal a later single-threaded call.
-
-The threads enqueue on ONE shared stream: two grouped-GEMM launches must not
-run on the device at the same time (the persistent GEMM's Linear-2 tiles wait
-on Linear-1 tiles of other CTAs, which assumes the whole grid is resident), so
-what races here is the host side, not the kernels."""
+first layer calls of the process at the same time, each on its own stream with
+its own inputs and workspace, so the library's one-time per-device launch setup
+races and the persistent grouped GEMMs of different calls share the GPU (each
+gets whatever SMs are free; tiles are claimed in order by running CTAs, so no
+grid waits for CTAs that have not started); every result must equal a later
+single-threaded call."""
 import sys
 import threading
 
@@ -25,9 +23,7 @@ def main(n_threads: int) -> int:
         inp = synth.make_inputs(cfg, seed=10 + i, device="cuda")
         ws = moe.alloc_workspace(shape)
         out = [torch.empty(cfg.T // cfg.S, cfg.d, dtype=torch.bfloat16, device="cuda") for _ in range(cfg.S)]
-        jobs.append((shape, inp, ws, out))
-    shared = torch.cuda.Stream()
-    jobs = [j + (shared,) for j in jobs]
+        jobs.append((shape, inp, ws, out, torch.cuda.Stream()))
     torch.cuda.synchronize()
     start = threading.Barrier(n_threads)
     errors = []

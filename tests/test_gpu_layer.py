@@ -139,10 +139,10 @@ def test_layer_replays_from_a_cuda_graph(cfg):
 
 
 def test_first_calls_from_several_threads_at_once():
-    """The one-time per-device launch setup is thread safe: in a fresh process,
-    four threads start their first layer calls together (each with its own
-    inputs and workspace, on one shared stream, since two grouped GEMMs must
-    not run on the device at once) and all get the single-threaded result."""
+    """The one-time per-device launch setup is thread safe and grouped GEMMs of
+    different calls may share the GPU: in a fresh process, four threads start
+    their first layer calls together (each with its own stream, inputs and
+    workspace) and all get the single-threaded result."""
     need_gpu()
     import subprocess
     import sys
@@ -282,3 +282,30 @@ def test_tile_timeline_records_every_tile_once():
             got.append((int(w[0] & 3), int((w[0] >> 2) & 0xFFFFFFFF), int(w[0] >> 34)))
             assert w[1] > 0 and w[3] <= w[4] <= w[7], w
     assert sorted(got) == expected
+
+
+def test_overlapping_layers_on_two_streams():
+    """Two streams each run layer calls back to back, so their persistent
+    grouped GEMMs (one CTA pair per SM each) share the GPU and each grid gets
+    only part of the SMs at times; tiles are claimed in order by running CTAs,
+    so both complete, with the results of separate calls."""
+    need_gpu()
+    cfgs = [synth.CONFIGS["mid"], custom_cfg(8192, 1024, 16, 2, 2048, zipf_s=1.0)]
+    layers = [GpuLayer(c, seed=5 + i) for i, c in enumerate(cfgs)]
+    ref = [layer.forward().clone() for layer in layers]
+    streams = [torch.cuda.Stream() for _ in layers]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for layer in layers:
+            for o in layer.out:
+                o.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for rep in range(3):
+            for layer, st in zip(layers, streams):
+                i = layer.inp
+                moe.layer_forward(layer.shape, i.x, i.wr, i.bias, i.w1, i.w3, i.w2, layer.out, layer.ws,
+                                  stream=st)
+        torch.cuda.synchronize()
+        for layer, st, r in zip(layers, streams, ref):
+            assert moe.last_device_status(layer.ws, st) == moe.MOE_OK, moe.last_device_detail()
+            assert torch.equal(torch.cat(layer.out, 0).view(torch.int16), r.view(torch.int16))
