@@ -8,17 +8,24 @@
 //   topk_gate[t,:]= softmax over those k logits
 //
 // Logits are computed on CUDA cores in fp32 (tensor cores are kept for the
-// expert GEMMs). Each logit is accumulated by ONE thread in ascending i with
-// fmaf: every bf16 x bf16 product is exact in fp32, so the result is the fp32
-// sequential sum, rounded once per addition, independent of the tiling. The
-// selection is therefore reproducible bit for bit by any implementation of
-// that sum.
+// expert GEMMs). Each logit is accumulated by ONE thread in ascending i, one
+// fused multiply-add per feature: every bf16 x bf16 product is exact in fp32,
+// so the result is the fp32 sequential sum, rounded once per addition,
+// independent of the tiling. The selection is therefore reproducible bit for
+// bit by any implementation of that sum.
 //
-// Block tile: BT tokens x BE >= E experts, staged through shared memory a
-// chunk of features at a time as fp32 rows (the next chunk is prefetched into registers
-// while the current one is used), each thread owning TM tokens x TN experts.
-// Then one warp per token runs k rounds of a shuffle arg-max over the block's
-// logits and writes idx and gates.
+// Kernels, by expert count (each thread owns TM tokens x TN experts of a
+// block tile; the tiles of x and the weights pass through shared memory a
+// chunk of features at a time):
+//   E > 128, 33..64   route_kernel_bf16: bf16 tiles in a cp.async ring, the
+//                     mixed-precision FMA (bf16 operands, fp32 accumulator)
+//   9..16             route_kernel_resident: weights resident per block,
+//                     per-warp rings over 32-token tasks, selection in lane
+//                     (when the weights fit; else route_kernel)
+//   65..128, 17..32   route_kernel: fp32 tiles, register prefetch
+//   <= 8              route_kernel_async: bf16 ring widened at use
+// Except in route_kernel_resident, one warp per token then runs k rounds of a
+// shuffle arg-max over the block's logits and writes idx and gates.
 #include <cuda_bf16.h>
 #include <float.h>
 
@@ -27,6 +34,7 @@
 namespace moe {
 namespace {
 
+constexpr size_t kMaxSmemPerBlock = 232448;  // opt-in shared memory per block (227 KB)
 
 struct RouteParams {
     const uint16_t *x;
@@ -357,171 +365,6 @@ __global__ void __launch_bounds__(32 * WE * WT) route_kernel_async(const RoutePa
     select_topk<BE, NW>(p, lg, t0, BT, warp, lane);
 }
 
-// Large expert counts (E > 128), where the router is bound by the fp32 FMA
-// rate. Same thread layout and accumulation as route_kernel, but the staging
-// holds no registers: each chunk of kBK features is copied raw (bf16, 16-byte
-// cp.async, zero-filled past the end) into a shared-memory buffer while the
-// previous chunk is in use, then all threads widen it into the fp32 tiles in
-// one pass. The registers this frees let three blocks share an SM for the
-// smaller token tiles, and the FMAs of a 4-feature step run feature by
-// feature over the whole TM x TN tile, so consecutive FMAs never depend on
-// each other.
-template <int TM, int TN, int WE, int WT, int kBK>
-__global__ void __launch_bounds__(32 * WE * WT, TM <= 6 ? 3 : 2) route_kernel_cvt(const RouteParams p)
-{
-    constexpr int NT = 32 * WE * WT;
-    constexpr int BT = WT * 8 * TM;  // tokens per block
-    constexpr int BE = WE * 4 * TN;  // experts per block (>= E)
-    constexpr int NW = NT / 32;
-    constexpr int LD = kBK + 4;      // padded fp32 row (floats)
-    constexpr int RLD = kBK + 8;     // padded raw row (bf16): 16-byte aligned rows
-    constexpr int CPR = kBK / 8;     // 16-byte pieces per row
-    constexpr int ROWS = BT + BE;
-    extern __shared__ __align__(16) float rsm[];
-    float *xs = rsm;                                                // [BT][LD]
-    float *ws = rsm + BT * LD;                                      // [BE][LD]
-    uint16_t *raw = reinterpret_cast<uint16_t *>(rsm + ROWS * LD);  // [ROWS][RLD]
-    float *lg = rsm;                                                // [BT][BE + 1] after the K loop
-    pdl_wait();
-    pdl_trigger();
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int a = lane & 7, b = lane >> 3;
-    const int eb = (warp % WE) * 4 * TN, tb = (warp / WE) * 8 * TM;
-    const long t0 = static_cast<long>(blockIdx.x) * BT;
-    const int nchunks = (p.d + kBK - 1) / kBK;
-
-    auto issue = [&](int chunk) {
-        const int k0 = chunk * kBK;
-        for (int v = tid; v < ROWS * CPR; v += NT) {
-            const int r = v / CPR, c8 = (v % CPR) * 8;
-            const bool is_x = r < BT;
-            const long row = is_x ? t0 + r : static_cast<long>(r - BT);
-            const bool ok = k0 + c8 < p.d && (is_x ? row < p.T : row < p.E);
-            const uint16_t *src = is_x ? p.x + (ok ? row * p.d + k0 + c8 : 0)
-                                       : p.wr + (ok ? row * p.d + k0 + c8 : 0);
-            cp_async_16(raw + r * RLD + c8, src, ok);
-        }
-    };
-    auto widen_chunk = [&]() {
-        const uint16_t *st = raw;
-        for (int v = tid; v < ROWS * CPR; v += NT) {
-            const int r = v / CPR, c8 = (v % CPR) * 8;
-            const uint4 q = *reinterpret_cast<const uint4 *>(st + r * RLD + c8);
-            float *dst = r < BT ? xs + r * LD + c8 : ws + (r - BT) * LD + c8;
-            *reinterpret_cast<float4 *>(dst) =
-                make_float4(bf16_bits_to_f32(q.x & 0xFFFFu), bf16_bits_to_f32(q.x >> 16),
-                            bf16_bits_to_f32(q.y & 0xFFFFu), bf16_bits_to_f32(q.y >> 16));
-            *reinterpret_cast<float4 *>(dst + 4) =
-                make_float4(bf16_bits_to_f32(q.z & 0xFFFFu), bf16_bits_to_f32(q.z >> 16),
-                            bf16_bits_to_f32(q.w & 0xFFFFu), bf16_bits_to_f32(q.w >> 16));
-        }
-    };
-
-    float acc[TM][TN];
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
-
-    issue(0);
-    cp_async_commit();
-    for (int c = 0; c < nchunks; ++c) {
-        cp_async_wait<0>();  // chunk c has landed (the only copies in flight)
-        __syncthreads();     // ... for every thread, and chunk c - 1's tiles are no longer read
-        widen_chunk();
-        __syncthreads();     // tiles of chunk c ready; the raw buffer is free again
-        if (c + 1 < nchunks) issue(c + 1);  // lands while chunk c is used
-        cp_async_commit();
-#pragma unroll 2
-        for (int kk = 0; kk < kBK; kk += 4) {
-            float4 xv[TM], wv[TN];
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-                xv[i] = *reinterpret_cast<const float4 *>(xs + (tb + a + 8 * i) * LD + kk);
-#pragma unroll
-            for (int j = 0; j < TN; ++j)
-                wv[j] = *reinterpret_cast<const float4 *>(ws + (eb + b + 4 * j) * LD + kk);
-            // ascending feature order for every (token, expert) accumulator
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].x, wv[j].x, acc[i][j]);
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].y, wv[j].y, acc[i][j]);
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].z, wv[j].z, acc[i][j]);
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(xv[i].w, wv[j].w, acc[i][j]);
-        }
-    }
-    __syncthreads();  // every thread is done with the tiles before the logits overwrite them
-
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-#pragma unroll
-        for (int j = 0; j < TN; ++j) {
-            const int e = eb + b + 4 * j;
-            float z = acc[i][j];
-            if (p.bias != nullptr && e < p.E) z = z + p.bias[e];
-            lg[(tb + a + 8 * i) * (BE + 1) + e] = z;
-        }
-    }
-    __syncthreads();
-    select_topk<BE, NW>(p, lg, t0, BT, warp, lane);
-}
-
-template <int TM, int TN, int WE, int WT, int kBK>
-struct CvtVariant {
-    static constexpr int NT = 32 * WE * WT;
-    static constexpr int BT = WT * 8 * TM;
-    static constexpr int BE = WE * 4 * TN;
-    static constexpr size_t tiles =
-        sizeof(float) * (kBK + 4) * (BT + BE) + sizeof(uint16_t) * (BT + BE) * (kBK + 8);
-    static constexpr size_t logits = sizeof(float) * BT * (BE + 1);
-    static constexpr size_t smem = tiles > logits ? tiles : logits;
-
-    // once per device: the shared-memory attribute, and how many blocks fit
-    // on an SM (registers and shared memory); 0 when the setup failed
-    static int blocks_per_sm()
-    {
-        struct Tag {};
-        static int occ[kOnceDevices];
-        const cudaError_t e = once_per_device<Tag>([](int dev) {
-            cudaError_t err = cudaFuncSetAttribute(route_kernel_cvt<TM, TN, WE, WT, kBK>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem));
-            if (err != cudaSuccess) return err;
-            int n = 0;
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_kernel_cvt<TM, TN, WE, WT, kBK>, NT,
-                                                                smem);
-            if (err == cudaSuccess && dev >= 0 && dev < kOnceDevices) occ[dev] = n;
-            return err;
-        });
-        if (e != cudaSuccess) return 0;
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kOnceDevices) return 1;
-        return occ[dev];
-    }
-
-    static cudaError_t launch(const RouteParams &p, cudaStream_t s)
-    {
-        if (blocks_per_sm() <= 0) {
-            const cudaError_t e = cudaGetLastError();
-            return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-        }
-        const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
-        return launch_pdl(route_kernel_cvt<TM, TN, WE, WT, kBK>, dim3(grid), dim3(NT), smem, s, p);
-    }
-};
-
 template <int TM, int TN, int WE, int WT, int kBK>
 cudaError_t launch_variant(const RouteParams &p, cudaStream_t s)
 {
@@ -560,6 +403,363 @@ cudaError_t launch_variant_async(const RouteParams &p, cudaStream_t s)
     return launch_pdl(route_kernel_async<TM, TN, WE, WT, KB, STAGES>, dim3(grid), dim3(NT), smem, s, p);
 }
 
+// Mixed-precision FMA: d = a * b + c with a and b bf16 and c, d fp32. The
+// product of two bf16 values is exact in fp32 and the sum is rounded once
+// (round to nearest even), so the result equals fmaf on the widened operands
+// bit for bit, subnormals included; it saves the widening instructions and
+// lets x and the router weights stay bf16 in shared memory (PTX ISA, "fma",
+// mixed-precision form with .f32 destination and .bf16 sources).
+__device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c)
+{
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(c) : "h"(a), "h"(b));
+    return c;
+}
+
+// Half g (0..7, ascending feature) of eight packed bf16 values.
+__device__ __forceinline__ uint16_t bf16_half(const uint4 &q, int g)
+{
+    const uint32_t w = g < 2 ? q.x : g < 4 ? q.y : g < 6 ? q.z : q.w;
+    return static_cast<uint16_t>((g & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+// Large expert counts (E > 128) and the 33..64 range: the router is bound by
+// the fp32 FMA issue rate and, with fp32 tiles, by shared-memory bandwidth.
+// Same thread layout and accumulation order as route_kernel, but x and the
+// weights stay raw bf16 (16-byte cp.async, zero-filled past the end) in an
+// S-deep ring of kBK-feature chunks and feed fma_bf16: half the shared-memory
+// bytes per value and no widening pass. TM <= 6 fits three blocks per SM.
+template <int TM, int TN, int WE, int WT, int kBK, int S>
+__global__ void __launch_bounds__(32 * WE * WT, TM <= 6 ? 3 : 2) route_kernel_bf16(const RouteParams p)
+{
+    constexpr int NT = 32 * WE * WT;
+    constexpr int BT = WT * 8 * TM;  // tokens per block
+    constexpr int BE = WE * 4 * TN;  // experts per block (>= E)
+    constexpr int NW = NT / 32;
+    constexpr int RLD = kBK + 8;     // padded bf16 row: 16-byte aligned, rows 4 banks apart
+    constexpr int CPR = kBK / 8;     // 16-byte pieces per row
+    constexpr int ROWS = BT + BE;
+    extern __shared__ __align__(16) float rsm[];
+    uint16_t *raw = reinterpret_cast<uint16_t *>(rsm);  // [S][ROWS][RLD]
+    float *lg = rsm;                                     // [BT][BE + 1] after the K loop
+    pdl_wait();
+    pdl_trigger();
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int a = lane & 7, b = lane >> 3;
+    const int eb = (warp % WE) * 4 * TN, tb = (warp / WE) * 8 * TM;
+    const long t0 = static_cast<long>(blockIdx.x) * BT;
+    const int nchunks = (p.d + kBK - 1) / kBK;
+
+    auto issue = [&](int chunk) {
+        const int k0 = chunk * kBK;
+        uint16_t *st = raw + (chunk % S) * ROWS * RLD;
+        for (int v = tid; v < ROWS * CPR; v += NT) {
+            const int r = v / CPR, c8 = (v % CPR) * 8;
+            const bool is_x = r < BT;
+            const long row = is_x ? t0 + r : static_cast<long>(r - BT);
+            const bool ok = k0 + c8 < p.d && (is_x ? row < p.T : row < p.E);
+            const uint16_t *src = is_x ? p.x + (ok ? row * p.d + k0 + c8 : 0)
+                                       : p.wr + (ok ? row * p.d + k0 + c8 : 0);
+            cp_async_16(st + r * RLD + c8, src, ok);
+        }
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+    for (int c = 0; c < S - 1; ++c) {
+        if (c < nchunks) issue(c);
+        cp_async_commit();
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        cp_async_wait<S - 2>();
+        __syncthreads();  // chunk c landed for every thread; chunk c - 1's slot is free
+        if (c + S - 1 < nchunks) issue(c + S - 1);
+        cp_async_commit();
+        const uint16_t *st = raw + (c % S) * ROWS * RLD;
+        const uint16_t *xs = st + (tb + a) * RLD;
+        const uint16_t *ws = st + (BT + eb + b) * RLD;
+#pragma unroll 1
+        for (int kk = 0; kk < kBK; kk += 8) {
+            uint4 xq[TM], wq[TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) xq[i] = *reinterpret_cast<const uint4 *>(xs + 8 * i * RLD + kk);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) wq[j] = *reinterpret_cast<const uint4 *>(ws + 4 * j * RLD + kk);
+#pragma unroll
+            for (int g = 0; g < 8; ++g)  // ascending feature order for every accumulator
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const uint16_t xh = bf16_half(xq[i], g);
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fma_bf16(xh, bf16_half(wq[j], g), acc[i][j]);
+                }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // every thread is done with the ring before the logits overwrite it
+
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int e = eb + b + 4 * j;
+            float z = acc[i][j];
+            if (p.bias != nullptr && e < p.E) z = z + p.bias[e];
+            lg[(tb + a + 8 * i) * (BE + 1) + e] = z;
+        }
+    }
+    __syncthreads();
+    select_topk<BE, NW>(p, lg, t0, BT, warp, lane);
+}
+
+template <int TM, int TN, int WE, int WT, int kBK, int S>
+struct Bf16Variant {
+    static constexpr int NT = 32 * WE * WT;
+    static constexpr int BT = WT * 8 * TM;
+    static constexpr int BE = WE * 4 * TN;
+    static constexpr size_t tiles = sizeof(uint16_t) * S * (BT + BE) * (kBK + 8);
+    static constexpr size_t logits = sizeof(float) * BT * (BE + 1);
+    static constexpr size_t smem = tiles > logits ? tiles : logits;
+
+    // once per device: the shared-memory attribute, and how many blocks fit
+    // on an SM (registers and shared memory); 0 when the setup failed
+    static int blocks_per_sm()
+    {
+        struct Tag {};
+        static int occ[kOnceDevices];
+        const cudaError_t e = once_per_device<Tag>([](int dev) {
+            cudaError_t err = cudaFuncSetAttribute(route_kernel_bf16<TM, TN, WE, WT, kBK, S>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+            if (err != cudaSuccess) return err;
+            int n = 0;
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_kernel_bf16<TM, TN, WE, WT, kBK, S>, NT,
+                                                                smem);
+            if (err == cudaSuccess && dev >= 0 && dev < kOnceDevices) occ[dev] = n;
+            return err;
+        });
+        if (e != cudaSuccess) return 0;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kOnceDevices) return 1;
+        return occ[dev];
+    }
+
+    static cudaError_t launch(const RouteParams &p, cudaStream_t s)
+    {
+        if (blocks_per_sm() <= 0) {
+            const cudaError_t e = cudaGetLastError();
+            return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+        }
+        const unsigned grid = static_cast<unsigned>((p.T + BT - 1) / BT);
+        return launch_pdl(route_kernel_bf16<TM, TN, WE, WT, kBK, S>, dim3(grid), dim3(NT), smem, s, p);
+    }
+};
+
+// Top-k and softmax of one token whose BE logits sit in the calling lane,
+// giving exactly what select_topk gives for them: the arg-max with ties to
+// the lower index is unique for finite logits whatever the scan order, and
+// the exponential sum pairs the same terms as select_topk's butterfly (xor
+// distances 16, 8, 4, 2, 1 over lanes j < k holding choice j: the steps at
+// distance 16 and 8 add exact zeros or pair j with j + 8, then j + 4, j + 2,
+// j + 1), so every rounding matches.
+template <int BE>
+__device__ __forceinline__ void select_topk_lane(const RouteParams &p, const float *z, long t)
+{
+    static_assert(BE == 16, "the pairing below is written for 16 logits");
+    uint32_t avail = p.E >= 32 ? 0xFFFFFFFFu : (1u << p.E) - 1u;
+    float ev[BE];
+    float zmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < BE; ++j) {
+        ev[j] = 0.0f;
+        if (j < p.k) {
+            float bv = -FLT_MAX;
+            int be = -1;
+#pragma unroll
+            for (int e = 0; e < BE; ++e)
+                if (((avail >> e) & 1u) && (be < 0 || z[e] > bv)) {
+                    bv = z[e];
+                    be = e;
+                }
+            avail &= ~(1u << be);
+            if (j == 0) zmax = bv;
+            ev[j] = expf(bv - zmax);
+            p.idx[t * p.k + j] = be;
+        }
+    }
+    float s8[8], s4[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s8[i] = ev[i] + ev[i + 8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s4[i] = s8[i] + s8[i + 4];
+    const float den = (s4[0] + s4[2]) + (s4[1] + s4[3]);
+#pragma unroll
+    for (int j = 0; j < BE; ++j)
+        if (j < p.k) p.gate[t * p.k + j] = ev[j] / den;
+}
+
+// E <= 16 with a short feature dimension (the weights fit in shared memory):
+// the block keeps all router weights resident (bf16, rows padded by 16
+// bytes) for its whole life, and each warp runs its own cp.async ring over
+// 32-token tasks b + G * (w + NWARP * i) of a grid of G blocks, so no block
+// barrier sits in the main loop and every SM's warps share out the tasks.
+// Lane (a, b) = (lane & 7, lane >> 3) owns tokens a + 8i and experts b + 4j
+// (i, j < 4): each value read from shared memory feeds four FMAs. The 16
+// logits of a token meet in a per-warp buffer, then the token's lane selects.
+template <int NWARP, int KB, int STAGES>
+__global__ void __launch_bounds__(32 * NWARP, 1) route_kernel_resident(const RouteParams p)
+{
+    constexpr int BE = 16;
+    constexpr int NT = 32 * NWARP;
+    constexpr int XLD = KB + 8;   // padded bf16 row of x
+    constexpr int CPR = KB / 8;
+    constexpr int RING = STAGES * 32 * XLD;
+    extern __shared__ __align__(16) float rsm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int la = lane & 7, lb = lane >> 3;
+    const int nchunks = (p.d + KB - 1) / KB;
+    const int WLD = nchunks * KB + 8;                                // padded bf16 weight row, zero past d
+    uint16_t *wsb = reinterpret_cast<uint16_t *>(rsm);               // [BE][WLD]
+    float *lg = rsm + BE * WLD / 2 + warp * 32 * (BE + 1);           // [32][BE + 1] per warp
+    uint16_t *ring = reinterpret_cast<uint16_t *>(rsm + BE * WLD / 2 + NWARP * 32 * (BE + 1)) + warp * RING;
+    pdl_wait();
+    pdl_trigger();
+
+    const long ntasks = (p.T + 31) / 32;
+    const long G = gridDim.x;
+    const long stride = G * NWARP;
+    const long first = blockIdx.x + G * warp;
+    const long my_tasks = first < ntasks ? (ntasks - 1 - first) / stride + 1 : 0;
+    const long nq = my_tasks * nchunks;  // this warp's chunks, task after task
+    auto issue = [&](long q) {
+        const long t0 = (first + (q / nchunks) * stride) * 32;
+        const int k0 = static_cast<int>(q % nchunks) * KB;
+        uint16_t *st = ring + static_cast<int>(q % STAGES) * 32 * XLD;
+#pragma unroll
+        for (int v = lane; v < 32 * CPR; v += 32) {
+            const int r = v / CPR, c8 = (v % CPR) * 8;
+            const long row = t0 + r;
+            const bool ok = k0 + c8 < p.d && row < p.T;
+            cp_async_16(st + r * XLD + c8, p.x + (ok ? row * p.d + k0 + c8 : 0), ok);
+        }
+    };
+#pragma unroll
+    for (int q = 0; q < STAGES - 1; ++q) {
+        if (q < nq) issue(q);
+        cp_async_commit();
+    }
+    // the weights, eight 16-byte loads in flight per thread before any store
+    {
+        const int rowv = WLD / 8, nv = BE * rowv;
+        for (int v0 = 0; v0 < nv; v0 += 8 * NT) {
+            uint4 w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * NT + tid;
+                const int e = v / rowv, c = (v % rowv) * 8;
+                w[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (v < nv && e < p.E && c < p.d)
+                    w[u] = *reinterpret_cast<const uint4 *>(p.wr + static_cast<long>(e) * p.d + c);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * NT + tid;
+                if (v < nv) {
+                    const int e = v / rowv, c = (v % rowv) * 8;
+                    *reinterpret_cast<uint4 *>(wsb + e * WLD + c) = w[u];
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    float acc[4][4];
+    for (long q = 0; q < nq; ++q) {
+        const int c = static_cast<int>(q % nchunks);
+        if (c == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+        }
+        cp_async_wait<STAGES - 2>();
+        __syncwarp();  // chunk q landed for every lane; chunk q - 1's slot is free
+        if (q + STAGES - 1 < nq) issue(q + STAGES - 1);
+        cp_async_commit();
+        const uint16_t *xs = ring + static_cast<int>(q % STAGES) * 32 * XLD + la * XLD;
+        const uint16_t *wc = wsb + lb * WLD + c * KB;
+#pragma unroll 2
+        for (int kk = 0; kk < KB; kk += 8) {
+            uint4 xq[4], wq[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xq[i] = *reinterpret_cast<const uint4 *>(xs + 8 * i * XLD + kk);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wq[j] = *reinterpret_cast<const uint4 *>(wc + 4 * j * WLD + kk);
+#pragma unroll
+            for (int g = 0; g < 8; ++g)  // ascending feature order
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint16_t xh = bf16_half(xq[i], g);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fma_bf16(xh, bf16_half(wq[j], g), acc[i][j]);
+                }
+        }
+        if (c == nchunks - 1) {
+            const long t0 = (first + (q / nchunks) * stride) * 32;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) lg[(la + 8 * i) * (BE + 1) + lb + 4 * j] = acc[i][j];
+            __syncwarp();
+            const long t = t0 + lane;
+            if (t < p.T) {
+                float z[BE];
+#pragma unroll
+                for (int e = 0; e < BE; ++e) {
+                    z[e] = lg[lane * (BE + 1) + e];
+                    if (p.bias != nullptr && e < p.E) z[e] = z[e] + p.bias[e];
+                }
+                select_topk_lane<BE>(p, z, t);
+            }
+            __syncwarp();  // the buffer is rewritten by the next task
+        }
+    }
+    cp_async_wait<0>();
+}
+
+// Shared memory of route_kernel_resident for d features; 0 when it does not
+// fit in one block.
+template <int NWARP, int KB, int STAGES>
+size_t resident_smem(int d)
+{
+    const size_t nchunks = (static_cast<size_t>(d) + KB - 1) / KB;
+    const size_t bytes = sizeof(uint16_t) * 16 * (nchunks * KB + 8) + sizeof(float) * NWARP * 32 * 17 +
+                         sizeof(uint16_t) * NWARP * STAGES * 32 * (KB + 8);
+    return bytes <= kMaxSmemPerBlock ? bytes : 0;
+}
+
+template <int NWARP, int KB, int STAGES>
+cudaError_t launch_resident(const RouteParams &p, size_t smem, cudaStream_t s)
+{
+    struct Tag {};
+    const cudaError_t e = once_per_device<Tag>([](int) {
+        return cudaFuncSetAttribute(route_kernel_resident<NWARP, KB, STAGES>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxSmemPerBlock));
+    });
+    if (e != cudaSuccess) return e;
+    const long ntasks = (p.T + 31) / 32;
+    const long sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    const unsigned grid = static_cast<unsigned>(ntasks < sms ? ntasks : sms);
+    return launch_pdl(route_kernel_resident<NWARP, KB, STAGES>, dim3(grid), dim3(32 * NWARP), smem, s, p);
+}
+
+
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
@@ -572,13 +772,15 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
         // BE 256 as 4 warps x 4 expert lanes x 16 experts per thread (128
         // threads), TM tokens per thread. The token tile (8 * TM tokens) is
         // the one whose last wave of blocks is fullest, counting the blocks
-        // that fit on an SM for each tile (TM <= 6 needs ~170 registers, so
-        // three blocks fit; TM 7-8 take up to 255, two blocks), slightly
+        // that fit on an SM for each tile (TM <= 6 keeps to ~170 registers,
+        // so three blocks fit; TM 7-8 take up to 255, two blocks), slightly
         // favouring larger tiles (more reuse of each staged feature chunk).
         const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
-        const int occ[5] = {CvtVariant<4, 16, 4, 1, 32>::blocks_per_sm(), CvtVariant<5, 16, 4, 1, 32>::blocks_per_sm(),
-                            CvtVariant<6, 16, 4, 1, 32>::blocks_per_sm(), CvtVariant<7, 16, 4, 1, 32>::blocks_per_sm(),
-                            CvtVariant<8, 16, 4, 1, 32>::blocks_per_sm()};
+        const int occ[5] = {Bf16Variant<4, 16, 4, 1, 32, 3>::blocks_per_sm(),
+                            Bf16Variant<5, 16, 4, 1, 32, 3>::blocks_per_sm(),
+                            Bf16Variant<6, 16, 4, 1, 32, 3>::blocks_per_sm(),
+                            Bf16Variant<7, 16, 4, 1, 32, 3>::blocks_per_sm(),
+                            Bf16Variant<8, 16, 4, 1, 32, 3>::blocks_per_sm()};
         int best_tm = 8;
         double best = -1.0;
         for (int tm = 8; tm >= 4; --tm) {
@@ -592,18 +794,22 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
             }
         }
         switch (best_tm) {
-        case 7: return CvtVariant<7, 16, 4, 1, 32>::launch(p, s);
-        case 6: return CvtVariant<6, 16, 4, 1, 32>::launch(p, s);
-        case 5: return CvtVariant<5, 16, 4, 1, 32>::launch(p, s);
-        case 4: return CvtVariant<4, 16, 4, 1, 32>::launch(p, s);
-        default: return CvtVariant<8, 16, 4, 1, 32>::launch(p, s);
+        case 7: return Bf16Variant<7, 16, 4, 1, 32, 3>::launch(p, s);
+        case 6: return Bf16Variant<6, 16, 4, 1, 32, 3>::launch(p, s);
+        case 5: return Bf16Variant<5, 16, 4, 1, 32, 3>::launch(p, s);
+        case 4: return Bf16Variant<4, 16, 4, 1, 32, 3>::launch(p, s);
+        default: return Bf16Variant<8, 16, 4, 1, 32, 3>::launch(p, s);
         }
     }
-    if (a.E > 64) return launch_variant<2, 8, 4, 2, 64>(p, s);    // BT 32, BE 128
-    if (a.E > 32) return launch_variant_async<2, 4, 4, 1, 128, 4>(p, s);  // BT 16, BE 64
-    if (a.E > 16) return launch_variant<2, 2, 4, 2, 128>(p, s);           // BT 32, BE 32
-    if (a.E > 8) return launch_variant<2, 4, 1, 8, 128>(p, s);            // BT 128, BE 16
-    return launch_variant_async<1, 1, 2, 4, 128, 4>(p, s);                // BT 32, BE 8
+    if (a.E > 64) return launch_variant<2, 8, 4, 2, 64>(p, s);                  // BT 32, BE 128
+    if (a.E > 32) return Bf16Variant<2, 2, 8, 1, 64, 4>::launch(p, s);        // BT 16, BE 64
+    if (a.E > 16) return launch_variant<2, 2, 4, 2, 128>(p, s);                 // BT 32, BE 32
+    if (a.E > 8) {
+        // resident weights while they fit next to eight warps' rings
+        if (const size_t smem = resident_smem<8, 64, 4>(a.d)) return launch_resident<8, 64, 4>(p, smem, s);
+        return launch_variant<2, 4, 1, 8, 128>(p, s);                           // BT 128, BE 16
+    }
+    return launch_variant_async<1, 1, 2, 4, 128, 4>(p, s);                      // BT 32, BE 8
 }
 
 }  // namespace moe
