@@ -12,8 +12,9 @@
 //              chunk's slots; per-warp counts and a prefix over warps give each
 //              warp its bases; it then ranks equal experts 32 slots at a time
 //              with __match_any_sync and writes row_of_slot / slot_of_row
-//   4. copy    one warp per token: x[t] read once with 16-byte loads and
-//              written to its k destination rows
+//   4. copy    one warp per token: x[t] read once with 16-byte loads (the
+//              first 2048 features before the wait on rank) and written to
+//              its k destination rows
 #include "kernels.cuh"
 #include "sm100.cuh"
 
@@ -166,27 +167,45 @@ __global__ void __launch_bounds__(kThreads) rank_kernel(const int32_t *__restric
     }
 }
 
+// One warp per token. The first 2048 features of the token's row are loaded
+// before the wait on the rank kernel: x was complete before the first
+// dispatch kernel passed its own wait, and each kernel of the chain launches
+// only after every block of its predecessor passed that predecessor's wait,
+// so the x loads overlap the bookkeeping kernels; only the row map needs the
+// wait.
 __global__ void __launch_bounds__(kThreads) copy_kernel(const uint16_t *__restrict__ x,
                                                         const int32_t *__restrict__ row_of_slot,
                                                         int T, int d, int k, uint16_t *x_perm)
 {
-    pdl_wait();
+    constexpr int U = 8;  // 16-byte vectors per lane loaded ahead
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long t = static_cast<long>(blockIdx.x) * (kThreads / 32) + warp;
-    if (t >= T) return;
+    const bool live = t < T;
+    const int nvec = d / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (live ? t : 0) * d);
+    uint4 ahead[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int v = u * 32 + lane;
+        if (live && v < nvec) ahead[u] = src[v];
+    }
+    pdl_wait();
+    if (!live) return;
     int rows[kMaxTopK];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? row_of_slot[t * k + j] : 0;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d);
-    const int nvec = d / 8;
-    for (int v = lane; v < nvec; v += 32) {
-        const uint4 val = src[v];
+    for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? row_of_slot[t * k + j] : -1;
+    auto put = [&](int v, const uint4 &val) {
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k && rows[j] >= 0)
-                reinterpret_cast<uint4 *>(x_perm + static_cast<long>(rows[j]) * d)[v] = val;
+            if (j < k && rows[j] >= 0) reinterpret_cast<uint4 *>(x_perm + static_cast<long>(rows[j]) * d)[v] = val;
+    };
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int v = u * 32 + lane;
+        if (v < nvec) put(v, ahead[u]);
     }
+    for (int v = U * 32 + lane; v < nvec; v += 32) put(v, src[v]);
 }
 
 }  // namespace
