@@ -535,6 +535,9 @@ def run_ours(args, cfg):
     layer_frac = t_roof / (ms_per_step / 1000.0)
     layer_frac_sus = t_roof_sus / (ms_per_step / 1000.0)
 
+    stage_roofline = stage_rooflines(cfg, stage_ms, hbm, float(peaks.get("sm_max_mhz", 2070.0)),
+                                     torch.cuda.get_device_properties(dev).multi_processor_count)
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         nth = cpu_threads()
@@ -555,7 +558,7 @@ def run_ours(args, cfg):
         "layer_roofline_frac": layer_frac, "layer_roofline_frac_of_sustained": layer_frac_sus,
         "stage_ms": {"route": float(stage_ms[:, 0].mean()), "dispatch": float(stage_ms[:, 1].mean()),
                      "grouped_gemm": gemm_ms, "combine": float(stage_ms[:, 3].mean())},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "graph": graph,
+        "roofline": roofline, "stage_roofline": stage_roofline, "cpu_baseline": cpu, "e2e": e2e, "graph": graph,
         "gpu_launches": moe.layer_kernel_launches(shape, tuning) * args.steps, "clocks": clocks,
         "wall_s_timed": t_wall,
     }
@@ -591,6 +594,29 @@ def stage_bytes(cfg, stage):
     if stage == "dispatch":
         return 4.0 * R + 2.0 * T * d + 2.0 * R * d + 8.0 * R + 8.0 * E
     return 2.0 * R * d + 8.0 * R + 2.0 * T * d  # combine
+
+
+def stage_rooflines(cfg, stage_ms, hbm_gbs, sm_max_mhz, sms):
+    """Each layer stage other than the GEMM against its own ceiling, from the
+    stage events of the timed layer: achieved HBM bandwidth of its algorithmic
+    bytes (stage_bytes) for route, dispatch and combine, and for route also
+    the fp32 FMA rate (one logit is one thread's sequential sum on the CUDA
+    cores) against the nominal 128 FMA/clk per SM at the maximum SM clock."""
+    fp32_peak = sms * 128 * 2 * sm_max_mhz * 1e6 / 1e12
+    out = {}
+    for i, name in ((0, "route"), (1, "dispatch"), (3, "combine")):
+        sec = float(stage_ms[:, i].mean()) / 1000.0
+        gbs = stage_bytes(cfg, name) / sec / 1e9
+        rec = {"ms": sec * 1000.0, "hbm_gbs": gbs, "hbm_frac": gbs / hbm_gbs}
+        if name == "route":
+            tf = 2.0 * cfg.T * cfg.d * cfg.E / sec / 1e12
+            rec.update({"fp32_tflops": tf, "fp32_frac": tf / fp32_peak,
+                        "fp32_peak": fp32_peak, "fp32_peak_source": "nominal: SMs x 128 FMA/clk x max SM clock"})
+            rec["bound"] = "alu" if rec["fp32_frac"] > rec["hbm_frac"] else "hbm"
+        else:
+            rec["bound"] = "hbm"
+        out[name] = rec
+    return out
 
 
 def run_stage(args, cfg):
