@@ -45,26 +45,31 @@ template <int KMAX>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ gate,
                const int32_t *__restrict__ row_of_slot, int T, int d, int k, int rows_per_seg,
-               const Segments seg)
+               const Segments seg, int early_maps)
 {
     constexpr int U = 16 / KMAX;
-    pdl_wait();
+    // Inside the layer the row map and the gates come from kernels that
+    // finished before the grouped GEMM passed its own wait, so they are read
+    // before this kernel's wait; only y_perm needs it. Called on its own, the
+    // combine may follow the kernels that write them, and waits first.
+    if (!early_maps) pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long t = static_cast<long>(blockIdx.x) * (kThreads / 32) + warp;
-    if (t >= T) return;
     const uint4 *src[KMAX];
     float g[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
         // a slot whose expert id was out of range has no row (-1): no term;
         // neither has a row index past the T*k rows of y_perm
-        const int r = j < k ? row_of_slot[t * k + j] : -1;
+        const int r = (t < T && j < k) ? row_of_slot[t * k + j] : -1;
         src[j] = (r >= 0 && r < static_cast<long>(T) * k)
                      ? reinterpret_cast<const uint4 *>(y + static_cast<long>(r) * d)
                      : nullptr;
-        g[j] = j < k ? gate[t * k + j] : 0.0f;
+        g[j] = (t < T && j < k) ? gate[t * k + j] : 0.0f;
     }
+    if (early_maps) pdl_wait();
+    if (t >= T) return;
     uint4 *dst = reinterpret_cast<uint4 *>(seg.p[t / rows_per_seg] + (t % rows_per_seg) * static_cast<long>(d));
     const int nvec = d / 8;
     for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
@@ -101,12 +106,12 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s)
     const unsigned blocks = static_cast<unsigned>((a.T + kThreads / 32 - 1) / (kThreads / 32));
     if (a.k <= 2)
         return launch_pdl(combine_kernel<2>, dim3(blocks), dim3(kThreads), 0, s, a.y, a.gate, a.row_of_slot,
-                          a.T, a.d, a.k, a.T / a.S, seg);
+                          a.T, a.d, a.k, a.T / a.S, seg, a.early_maps ? 1 : 0);
     if (a.k <= 4)
         return launch_pdl(combine_kernel<4>, dim3(blocks), dim3(kThreads), 0, s, a.y, a.gate, a.row_of_slot,
-                          a.T, a.d, a.k, a.T / a.S, seg);
+                          a.T, a.d, a.k, a.T / a.S, seg, a.early_maps ? 1 : 0);
     return launch_pdl(combine_kernel<8>, dim3(blocks), dim3(kThreads), 0, s, a.y, a.gate, a.row_of_slot,
-                          a.T, a.d, a.k, a.T / a.S, seg);
+                          a.T, a.d, a.k, a.T / a.S, seg, a.early_maps ? 1 : 0);
 }
 
 }  // namespace moe

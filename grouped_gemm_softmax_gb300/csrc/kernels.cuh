@@ -108,6 +108,10 @@ struct CombineArgs {
     const int32_t *row_of_slot;
     uint16_t *seg[kMaxSegments];
     int T, d, k, S;
+    // the gates and the row map were complete before the kernel launched just
+    // ahead of the combine passed its own wait (the layer's grouped GEMM), so
+    // the combine may read them before its wait
+    bool early_maps;
 };
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 

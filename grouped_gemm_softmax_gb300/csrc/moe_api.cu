@@ -442,6 +442,7 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     ca.d = shape->d;
     ca.k = shape->top_k;
     ca.S = shape->num_segments;
+    ca.early_maps = true;  // the combine follows the grouped GEMM
     const bool fused = tuning && tuning->fused_combine;
     st = enqueue_ffn(shape, tuning, L, da.x_perm, da.offsets, W1, W3, W2,
                      region<uint16_t>(ws, L, MOE_WS_Y_PERM), ws, true, s, fused ? &ca : nullptr);
