@@ -116,6 +116,32 @@ def test_ragged_layers_every_token(cfg):
     _full_compare(layer, out, n_tokens=cfg.T, n_rows=cfg.R)
 
 
+def random_shape(E: int):
+    """A seeded random layer shape with E experts: T a multiple of S, d and F
+    multiples of 8 up to 384 (several K and N tiles, ragged tails), k up to
+    min(8, E), Zipf skew 0, 1 or 2."""
+    rng = np.random.default_rng(7000 + E)
+    k = int(rng.integers(1, min(8, E) + 1))
+    S = int(rng.choice([1, 2, 3, 8]))
+    T = int(rng.integers(1, 80)) * S
+    d = 8 * int(rng.integers(1, 49))
+    F = 8 * int(rng.integers(1, 49))
+    zipf = float(rng.choice([0.0, 1.0, 2.0]))
+    return custom_cfg(T, d, E, k, F, S=S, zipf_s=zipf)
+
+
+# one expert count per router kernel family (<= 8, 9..16, 17..32, 33..64,
+# 65..128, > 128) and their edges
+@pytest.mark.parametrize("E", [1, 3, 8, 9, 16, 17, 40, 64, 65, 130, 256])
+def test_random_shapes_every_token(E):
+    need_gpu()
+    cfg = random_shape(E)
+    print(f"E={E}: T={cfg.T} d={cfg.d} k={cfg.k} F={cfg.F} S={cfg.S} zipf={cfg.zipf_s}")
+    layer = GpuLayer(cfg, seed=E)
+    out = layer.forward()
+    _full_compare(layer, out, n_tokens=cfg.T, n_rows=cfg.R)
+
+
 @pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], custom_cfg(333, 256, 33, 4, 128, S=3, zipf_s=1.0)],
                          ids=["tiny", "T333_E33"])
 def test_layer_replays_from_a_cuda_graph(cfg):

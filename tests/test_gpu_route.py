@@ -43,7 +43,7 @@ def run_route(x, wr, bias, k):
     # fewer experts than the 16 logits a lane holds, more tasks than the
     # grid's warps (warps loop over tasks), and weights too large to keep
     (1000, 200, 16, 3, 1.0), (77, 520, 11, 4, 0.5), (40000, 64, 9, 8, 0.0), (100, 4096, 12, 2, 0.0),
-    (500, 2048, 16, 2, 0.0), (500, 2056, 16, 2, 0.0),
+    (500, 2048, 16, 2, 0.0), (500, 2056, 16, 2, 0.0), (1, 8, 12, 2, 0.0),
 ])
 def test_route_parity(T, d, E, k, zipf):
     need_gpu()
