@@ -19,11 +19,11 @@
 // chunk of features at a time):
 //   E > 128, 33..64   route_kernel_bf16: bf16 tiles in a cp.async ring, the
 //                     mixed-precision FMA (bf16 operands, fp32 accumulator)
-//   9..16             route_kernel_resident: weights resident per block,
-//                     per-warp rings over 32-token tasks, selection in lane
-//                     (when the weights fit; else route_kernel)
+//   <= 16             route_kernel_resident: weights resident per block,
+//                     per-warp rings over 32-token (9..16 experts) or 8-token
+//                     (<= 8) tasks, selection in lane (when the weights fit;
+//                     else route_kernel or route_kernel_async)
 //   65..128, 17..32   route_kernel: fp32 tiles, register prefetch
-//   <= 8              route_kernel_async: bf16 ring widened at use
 // Except in route_kernel_resident, one warp per token then runs k rounds of a
 // shuffle arg-max over the block's logits and writes idx and gates.
 #include <cuda_bf16.h>
@@ -571,13 +571,14 @@ struct Bf16Variant {
 template <int BE>
 __device__ __forceinline__ void select_topk_lane(const RouteParams &p, const float *z, long t)
 {
-    static_assert(BE == 16, "the pairing below is written for 16 logits");
+    static_assert(BE == 8 || BE == 16, "the pairing below covers up to 16 logits");
     uint32_t avail = p.E >= 32 ? 0xFFFFFFFFu : (1u << p.E) - 1u;
-    float ev[BE];
+    float ev[16];
     float zmax = 0.0f;
 #pragma unroll
+    for (int j = 0; j < 16; ++j) ev[j] = 0.0f;
+#pragma unroll
     for (int j = 0; j < BE; ++j) {
-        ev[j] = 0.0f;
         if (j < p.k) {
             float bv = -FLT_MAX;
             int be = -1;
@@ -607,42 +608,44 @@ __device__ __forceinline__ void select_topk_lane(const RouteParams &p, const flo
 // E <= 16 with a short feature dimension (the weights fit in shared memory):
 // the block keeps all router weights resident (bf16, rows padded by 16
 // bytes) for its whole life, and each warp runs its own cp.async ring over
-// 32-token tasks b + G * (w + NWARP * i) of a grid of G blocks, so no block
-// barrier sits in the main loop and every SM's warps share out the tasks.
-// Lane (a, b) = (lane & 7, lane >> 3) owns tokens a + 8i and experts b + 4j
-// (i, j < 4): each value read from shared memory feeds four FMAs. The 16
-// logits of a token meet in a per-warp buffer, then the token's lane selects.
-template <int NWARP, int KB, int STAGES>
+// BT-token tasks b + G * (w + NWARP * i) of a grid of G blocks (BT = 8 TM),
+// so no block barrier sits in the main loop and every SM's warps share out
+// the tasks. Lane (a, b) = (lane & 7, lane >> 3) owns tokens a + 8i (i < TM)
+// and experts b + 4j (j < BE / 4): each value read from shared memory feeds
+// several FMAs. The BE logits of a token meet in a per-warp buffer, then the
+// token's lane selects.
+template <int BE, int TM, int NWARP, int KB, int STAGES>
 __global__ void __launch_bounds__(32 * NWARP, 1) route_kernel_resident(const RouteParams p)
 {
-    constexpr int BE = 16;
+    constexpr int TN = BE / 4;    // experts per lane
+    constexpr int BT = 8 * TM;    // tokens per task
     constexpr int NT = 32 * NWARP;
     constexpr int XLD = KB + 8;   // padded bf16 row of x
     constexpr int CPR = KB / 8;
-    constexpr int RING = STAGES * 32 * XLD;
+    constexpr int RING = STAGES * BT * XLD;
     extern __shared__ __align__(16) float rsm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int la = lane & 7, lb = lane >> 3;
     const int nchunks = (p.d + KB - 1) / KB;
     const int WLD = nchunks * KB + 8;                                // padded bf16 weight row, zero past d
     uint16_t *wsb = reinterpret_cast<uint16_t *>(rsm);               // [BE][WLD]
-    float *lg = rsm + BE * WLD / 2 + warp * 32 * (BE + 1);           // [32][BE + 1] per warp
-    uint16_t *ring = reinterpret_cast<uint16_t *>(rsm + BE * WLD / 2 + NWARP * 32 * (BE + 1)) + warp * RING;
+    float *lg = rsm + BE * WLD / 2 + warp * BT * (BE + 1);           // [BT][BE + 1] per warp
+    uint16_t *ring = reinterpret_cast<uint16_t *>(rsm + BE * WLD / 2 + NWARP * BT * (BE + 1)) + warp * RING;
     pdl_wait();
     pdl_trigger();
 
-    const long ntasks = (p.T + 31) / 32;
+    const long ntasks = (p.T + BT - 1) / BT;
     const long G = gridDim.x;
     const long stride = G * NWARP;
     const long first = blockIdx.x + G * warp;
     const long my_tasks = first < ntasks ? (ntasks - 1 - first) / stride + 1 : 0;
     const long nq = my_tasks * nchunks;  // this warp's chunks, task after task
     auto issue = [&](long q) {
-        const long t0 = (first + (q / nchunks) * stride) * 32;
+        const long t0 = (first + (q / nchunks) * stride) * BT;
         const int k0 = static_cast<int>(q % nchunks) * KB;
-        uint16_t *st = ring + static_cast<int>(q % STAGES) * 32 * XLD;
+        uint16_t *st = ring + static_cast<int>(q % STAGES) * BT * XLD;
 #pragma unroll
-        for (int v = lane; v < 32 * CPR; v += 32) {
+        for (int v = lane; v < BT * CPR; v += 32) {
             const int r = v / CPR, c8 = (v % CPR) * 8;
             const long row = t0 + r;
             const bool ok = k0 + c8 < p.d && row < p.T;
@@ -679,46 +682,46 @@ __global__ void __launch_bounds__(32 * NWARP, 1) route_kernel_resident(const Rou
     }
     __syncthreads();
 
-    float acc[4][4];
+    float acc[TM][TN];
     for (long q = 0; q < nq; ++q) {
         const int c = static_cast<int>(q % nchunks);
         if (c == 0) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+                for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
         }
         cp_async_wait<STAGES - 2>();
         __syncwarp();  // chunk q landed for every lane; chunk q - 1's slot is free
         if (q + STAGES - 1 < nq) issue(q + STAGES - 1);
         cp_async_commit();
-        const uint16_t *xs = ring + static_cast<int>(q % STAGES) * 32 * XLD + la * XLD;
+        const uint16_t *xs = ring + static_cast<int>(q % STAGES) * BT * XLD + la * XLD;
         const uint16_t *wc = wsb + lb * WLD + c * KB;
 #pragma unroll 2
         for (int kk = 0; kk < KB; kk += 8) {
-            uint4 xq[4], wq[4];
+            uint4 xq[TM], wq[TN];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xq[i] = *reinterpret_cast<const uint4 *>(xs + 8 * i * XLD + kk);
+            for (int i = 0; i < TM; ++i) xq[i] = *reinterpret_cast<const uint4 *>(xs + 8 * i * XLD + kk);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) wq[j] = *reinterpret_cast<const uint4 *>(wc + 4 * j * WLD + kk);
+            for (int j = 0; j < TN; ++j) wq[j] = *reinterpret_cast<const uint4 *>(wc + 4 * j * WLD + kk);
 #pragma unroll
             for (int g = 0; g < 8; ++g)  // ascending feature order
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < TM; ++i) {
                     const uint16_t xh = bf16_half(xq[i], g);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fma_bf16(xh, bf16_half(wq[j], g), acc[i][j]);
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fma_bf16(xh, bf16_half(wq[j], g), acc[i][j]);
                 }
         }
         if (c == nchunks - 1) {
-            const long t0 = (first + (q / nchunks) * stride) * 32;
+            const long t0 = (first + (q / nchunks) * stride) * BT;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) lg[(la + 8 * i) * (BE + 1) + lb + 4 * j] = acc[i][j];
+                for (int j = 0; j < TN; ++j) lg[(la + 8 * i) * (BE + 1) + lb + 4 * j] = acc[i][j];
             __syncwarp();
             const long t = t0 + lane;
-            if (t < p.T) {
+            if (lane < BT && t < p.T) {
                 float z[BE];
 #pragma unroll
                 for (int e = 0; e < BE; ++e) {
@@ -735,30 +738,30 @@ __global__ void __launch_bounds__(32 * NWARP, 1) route_kernel_resident(const Rou
 
 // Shared memory of route_kernel_resident for d features; 0 when it does not
 // fit in one block.
-template <int NWARP, int KB, int STAGES>
+template <int BE, int TM, int NWARP, int KB, int STAGES>
 size_t resident_smem(int d)
 {
     const size_t nchunks = (static_cast<size_t>(d) + KB - 1) / KB;
-    const size_t bytes = sizeof(uint16_t) * 16 * (nchunks * KB + 8) + sizeof(float) * NWARP * 32 * 17 +
-                         sizeof(uint16_t) * NWARP * STAGES * 32 * (KB + 8);
+    const size_t bytes = sizeof(uint16_t) * BE * (nchunks * KB + 8) + sizeof(float) * NWARP * 8 * TM * (BE + 1) +
+                         sizeof(uint16_t) * NWARP * STAGES * 8 * TM * (KB + 8);
     return bytes <= kMaxSmemPerBlock ? bytes : 0;
 }
 
-template <int NWARP, int KB, int STAGES>
+template <int BE, int TM, int NWARP, int KB, int STAGES>
 cudaError_t launch_resident(const RouteParams &p, size_t smem, cudaStream_t s)
 {
     struct Tag {};
     const cudaError_t e = once_per_device<Tag>([](int) {
-        return cudaFuncSetAttribute(route_kernel_resident<NWARP, KB, STAGES>,
+        return cudaFuncSetAttribute(route_kernel_resident<BE, TM, NWARP, KB, STAGES>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxSmemPerBlock));
     });
     if (e != cudaSuccess) return e;
-    const long ntasks = (p.T + 31) / 32;
+    const long ntasks = (p.T + 8L * TM - 1) / (8L * TM);
     const long sms = device_sm_count() > 0 ? device_sm_count() : 1;
     const unsigned grid = static_cast<unsigned>(ntasks < sms ? ntasks : sms);
-    return launch_pdl(route_kernel_resident<NWARP, KB, STAGES>, dim3(grid), dim3(32 * NWARP), smem, s, p);
+    return launch_pdl(route_kernel_resident<BE, TM, NWARP, KB, STAGES>, dim3(grid), dim3(32 * NWARP), smem, s,
+                      p);
 }
-
 
 }  // namespace
 
@@ -806,9 +809,13 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s)
     if (a.E > 16) return launch_variant<2, 2, 4, 2, 128>(p, s);                 // BT 32, BE 32
     if (a.E > 8) {
         // resident weights while they fit next to eight warps' rings
-        if (const size_t smem = resident_smem<8, 64, 4>(a.d)) return launch_resident<8, 64, 4>(p, smem, s);
+        if (const size_t smem = resident_smem<16, 4, 8, 64, 4>(a.d))
+            return launch_resident<16, 4, 8, 64, 4>(p, smem, s);
         return launch_variant<2, 4, 1, 8, 128>(p, s);                           // BT 128, BE 16
     }
+    // E <= 8: resident weights, 8-token tasks (enough tasks for every SM even
+    // at a few thousand tokens) while they fit next to sixteen warps' rings
+    if (const size_t smem = resident_smem<8, 1, 16, 64, 8>(a.d)) return launch_resident<8, 1, 16, 64, 8>(p, smem, s);
     return launch_variant_async<1, 1, 2, 4, 128, 4>(p, s);                      // BT 32, BE 8
 }
 
