@@ -38,12 +38,14 @@ def run_route(x, wr, bias, k):
     # the fine layer, T = 16384, takes 7)
     (36, 64, 256, 8, 0.0), (43, 64, 256, 8, 0.0), (50, 64, 256, 8, 0.0), (57, 64, 256, 8, 0.0),
     (29, 64, 256, 8, 0.0), (8512, 64, 256, 8, 0.0), (12160, 64, 256, 8, 0.0),
-    # 9..16 experts keep the weights resident per block while they fit: a
-    # feature count off the 64-feature chunk, a ragged last 32-token task,
-    # fewer experts than the 16 logits a lane holds, more tasks than the
-    # grid's warps (warps loop over tasks), and weights too large to keep
+    # up to 16 experts keep the weights resident per block while they fit: a
+    # feature count off the 64-feature chunk, a ragged last task, fewer
+    # experts than the logits a lane holds, more tasks than the grid's warps
+    # (warps loop over tasks), and weights too large to keep (9..16 experts:
+    # d > 2048; up to 8: d > 4992)
     (1000, 200, 16, 3, 1.0), (77, 520, 11, 4, 0.5), (40000, 64, 9, 8, 0.0), (100, 4096, 12, 2, 0.0),
     (500, 2048, 16, 2, 0.0), (500, 2056, 16, 2, 0.0), (1, 8, 12, 2, 0.0),
+    (30000, 64, 5, 2, 1.0), (10, 4992, 8, 2, 0.0), (10, 5000, 8, 2, 0.0), (13, 72, 2, 2, 0.0),
 ])
 def test_route_parity(T, d, E, k, zipf):
     need_gpu()
