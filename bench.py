@@ -68,6 +68,8 @@ def parse_args():
                     help="CTAs per grouped-GEMM tile (0 = default)")
     ap.add_argument("--row-order", default="default", choices=["default", "expert", "mixed"],
                     help="order of the grouped GEMM's scheduler rows")
+    ap.add_argument("--router", default="default", choices=["default", "direct", "filter-verify"],
+                    help="how the layer routes (the same bits either way)")
     ap.add_argument("--fused-combine", action="store_true",
                     help="combine inside the grouped GEMM (consumer warps) instead of a separate kernel")
     ap.add_argument("--timeline", action="store_true",
@@ -353,7 +355,9 @@ def run_ours(args, cfg):
                         else moe.SCHEDULE_INTERLEAVED, lead_rows=args.lead, orientation=orient,
                         h_ring_rows=args.h_ring, fused_combine=1 if args.fused_combine else 0,
                         row_order={"default": 0, "expert": 1, "mixed": 2}[args.row_order],
-                        cta_group=args.cta_group, l2_block_n=args.l2_block_n)
+                        cta_group=args.cta_group, l2_block_n=args.l2_block_n,
+                        router={"default": moe.ROUTER_DEFAULT, "direct": moe.ROUTER_DIRECT,
+                                "filter-verify": moe.ROUTER_FILTER_VERIFY}[args.router])
     ws = moe.alloc_workspace(shape, dev, tuning if args.h_ring else None)
     rows = cfg.T // cfg.S
     out = [torch.empty(rows, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
@@ -595,6 +599,8 @@ def run_ours(args, cfg):
         line["config"]["l2_block_n"] = args.l2_block_n
     if args.row_order != "default":
         line["config"]["row_order"] = args.row_order
+    if args.router != "default":
+        line["config"]["router"] = args.router
     if args.fused_combine:
         line["config"]["fused_combine"] = True
     if args.h_ring:
@@ -669,8 +675,19 @@ def run_stage(args, cfg):
     if args.stage == "combine":
         y = xp  # the token rows stand in for the expert outputs
         segs = [torch.empty(cfg.T // cfg.S, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(cfg.S)]
+    # the route stage as the layer runs it: filter then verify by default above
+    # 128 experts (moe_route_filtered), else the direct kernels (moe_route)
+    filtered = args.router == "filter-verify" or (args.router == "default" and cfg.E > 128)
+    scratch = moe.alloc_route_scratch(shape, dev) if filtered else None
+
+    def route_call():
+        if filtered:
+            moe.route_filtered(shape, inp.x, inp.wr, inp.bias, idx, gate, scratch)
+        else:
+            moe.route(shape, inp.x, inp.wr, inp.bias, idx, gate)
+
     calls = {
-        "route": lambda: moe.route(shape, inp.x, inp.wr, inp.bias, idx, gate),
+        "route": route_call,
         "dispatch": lambda: moe.dispatch(shape, inp.x, idx, counts, offsets, ros, sor, xp, ws),
         "combine": lambda: moe.combine(shape, y, gate, ros, segs),
     }
@@ -691,8 +708,12 @@ def run_stage(args, cfg):
         if i >= args.warmup:
             ev.append((a, b))
     torch.cuda.synchronize()
+    if scratch is not None and moe.last_device_status(scratch) != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.last_device_detail()}")
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     conf = workload_config(cfg)
+    if args.stage == "route":
+        conf["router"] = "filter-verify" if filtered else "direct"
     conf["l2"] = ("flushed before every timed call (256 MiB write, then a 256 MiB read of another "
                   "buffer so the flush's write-back lands before the timed events)")
     line = {"stage": args.stage, "config": conf, "ms": ms, "steps": args.steps,

@@ -24,14 +24,16 @@ from .build import LIB_PATH
 
 __all__ = [
     "MoEError", "Shape", "Tuning", "library", "workspace_bytes", "workspace_region", "alloc_workspace",
-    "ws_view", "route", "dispatch", "expert_ffn", "combine", "layer_forward", "last_device_status",
+    "ws_view", "route", "route_scratch_bytes", "alloc_route_scratch", "route_filtered", "dispatch", "expert_ffn", "combine", "layer_forward", "last_device_status",
     "SCHEDULE_INTERLEAVED", "SCHEDULE_EXPERT_WAVE", "ORIENT_DEFAULT", "ORIENT_TOKENS_M", "ORIENT_TOKENS_N", "WS",
+    "ROUTER_DEFAULT", "ROUTER_DIRECT", "ROUTER_FILTER_VERIFY",
 ]
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = \
     range(6)
 SCHEDULE_INTERLEAVED, SCHEDULE_EXPERT_WAVE = 0, 1
 ORIENT_DEFAULT, ORIENT_TOKENS_M, ORIENT_TOKENS_N = 0, 1, 2
+ROUTER_DEFAULT, ROUTER_DIRECT, ROUTER_FILTER_VERIFY = 0, 1, 2
 
 
 class WS:
@@ -57,7 +59,8 @@ class _CTuning(ctypes.Structure):
                 ("wait_limit_us", ctypes.c_int), ("unmet_dependency", ctypes.c_int),
                 ("trace", ctypes.c_void_p), ("tile_trace", ctypes.c_void_p),
                 ("tile_trace_cap", ctypes.c_int), ("orientation", ctypes.c_int),
-                ("h_ring_rows", ctypes.c_int), ("fused_combine", ctypes.c_int), ("row_order", ctypes.c_int)]
+                ("h_ring_rows", ctypes.c_int), ("fused_combine", ctypes.c_int), ("row_order", ctypes.c_int),
+                ("router", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -103,6 +106,7 @@ class Tuning:
     h_ring_rows: int = 0  # h as a ring of this many scheduler rows (0 = all rows)
     fused_combine: int = 0  # layer only: combine inside the grouped GEMM (consumer warps)
     row_order: int = 0  # scheduler rows: 0 default, 1 expert order, 2 mixed (single-row experts spread out)
+    router: int = ROUTER_DEFAULT  # layer routing: ROUTER_DIRECT or ROUTER_FILTER_VERIFY (same bits)
 
     def c(self) -> _CTuning:
         tr = None if self.trace is None else _ptr(self.trace, torch.int64, None, "trace")
@@ -110,7 +114,7 @@ class Tuning:
         return _CTuning(self.schedule, self.lead_rows, self.num_ctas, self.l2_block_n, self.group_rows,
                         self.cta_group, self.wait_limit_us, self.unmet_dependency, tr, tt,
                         self.tile_trace_cap, self.orientation, self.h_ring_rows, self.fused_combine,
-                        self.row_order)
+                        self.row_order, self.router)
 
 
 _lib = None
@@ -135,6 +139,8 @@ def library():
             "moe_workspace_region_tuned": ([S, TU, ctypes.c_int, ctypes.POINTER(sz), ctypes.POINTER(sz)],
                                            ctypes.c_int),
             "moe_route": ([S, P, P, P, P, P, P], ctypes.c_int),
+            "moe_route_scratch_bytes": ([S], sz),
+            "moe_route_filtered": ([S, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "moe_dispatch": ([S, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "moe_expert_ffn": ([S, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "moe_expert_ffn_tuned": ([S, TU, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
@@ -254,6 +260,29 @@ def route(shape: Shape, x, w_router, expert_bias, topk_idx, topk_gate, stream=No
         _ptr(expert_bias, torch.float32, E, "expert_bias", optional=True),
         _ptr(topk_idx, torch.int32, T * k, "topk_idx"), _ptr(topk_gate, torch.float32, T * k, "topk_gate"),
         _stream(stream)), "moe_route")
+
+
+def route_scratch_bytes(shape: Shape) -> int:
+    return int(library().moe_route_scratch_bytes(ctypes.byref(shape.c())))
+
+
+def alloc_route_scratch(shape: Shape, device="cuda") -> torch.Tensor:
+    """Zeroed device scratch for route_filtered (its status word starts clear)."""
+    nb = route_scratch_bytes(shape)
+    if nb == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "invalid shape")
+    return torch.zeros(nb, dtype=torch.uint8, device=device)
+
+
+def route_filtered(shape: Shape, x, w_router, expert_bias, topk_idx, topk_gate, scratch, stream=None):
+    """route by filter then verify: the same bits in four launches (see moe.h)."""
+    T, d, E, k = shape.T, shape.d, shape.E, shape.top_k
+    _check(library().moe_route_filtered(
+        ctypes.byref(shape.c()), _ptr(x, torch.bfloat16, T * d, "x"),
+        _ptr(w_router, torch.bfloat16, E * d, "w_router"),
+        _ptr(expert_bias, torch.float32, E, "expert_bias", optional=True),
+        _ptr(topk_idx, torch.int32, T * k, "topk_idx"), _ptr(topk_gate, torch.float32, T * k, "topk_gate"),
+        _ptr(scratch, torch.uint8, None, "scratch"), scratch.numel(), _stream(stream)), "moe_route_filtered")
 
 
 def dispatch(shape: Shape, x, topk_idx, expert_counts, expert_offsets, row_of_slot, slot_of_row, x_perm,

@@ -51,6 +51,15 @@ struct RouteArgs {
 };
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
 
+// Filter-then-verify routing (route_tc.cu): the same results as launch_route
+// from four launches that sum exactly only the candidate experts. Needs
+// route_fast_scratch_bytes(T, E) bytes of 256-byte aligned device scratch and
+// the layer's status words (a bounded wait that runs out is recorded there).
+size_t route_fast_scratch_bytes(long T, int E);
+bool route_fast_supported(long T, int d, int E, int k);
+cudaError_t launch_route_fast(const RouteArgs &a, unsigned *status, void *scratch, size_t scratch_bytes,
+                              cudaStream_t s);
+
 struct DispatchArgs {
     const uint16_t *x;       // [T,d]
     const int32_t *topk_idx; // [T,k]

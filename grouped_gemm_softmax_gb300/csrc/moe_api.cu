@@ -56,6 +56,8 @@ struct Layout {
 };
 
 constexpr size_t kAlign = 1024;
+// moe_route_filtered's scratch: the status word, then route_tc.cu's scratch
+constexpr size_t kRouteStatusBytes = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -151,6 +153,7 @@ moe_status_t check_tuning(const moe_tuning_t *t)
         return MOE_ERR_INVALID_ARG;
     if (t->fused_combine < 0 || t->fused_combine > 1) return MOE_ERR_INVALID_ARG;
     if (t->row_order < 0 || t->row_order > 2) return MOE_ERR_INVALID_ARG;
+    if (t->router < 0 || t->router > 2) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -279,6 +282,35 @@ moe_status_t moe_route(const moe_shape_t *shape, const moe_bf16_t *x, const moe_
     return cuda_status(moe::launch_route(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_route_scratch_bytes(const moe_shape_t *shape)
+{
+    if (check_shape(shape) != MOE_OK) return 0;
+    return kRouteStatusBytes + moe::route_fast_scratch_bytes(shape->T, shape->E);
+}
+
+moe_status_t moe_route_filtered(const moe_shape_t *shape, const moe_bf16_t *x, const moe_bf16_t *w_router,
+                                const float *expert_bias, int32_t *topk_idx, float *topk_gate, void *scratch,
+                                size_t scratch_bytes, moe_stream_t stream)
+{
+    moe_status_t st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (shape->T == 0) return MOE_OK;
+    if (!x || !w_router || !topk_idx || !topk_gate || !scratch) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(topk_idx) || !aligned16(topk_gate) ||
+        (reinterpret_cast<uintptr_t>(scratch) & 255u) ||
+        (expert_bias && (reinterpret_cast<uintptr_t>(expert_bias) & 3u)))
+        return MOE_ERR_INVALID_ARG;
+    if (!moe::route_fast_supported(shape->T, shape->d, shape->E, shape->top_k)) return MOE_ERR_UNSUPPORTED;
+    if (scratch_bytes < moe_route_scratch_bytes(shape)) return MOE_ERR_WORKSPACE;
+    if (moe::encode_tiled_fn() == nullptr) return MOE_ERR_CUDA;
+    moe::RouteArgs a{x, w_router, expert_bias, topk_idx, topk_gate, shape->T, shape->d, shape->E,
+                     shape->top_k};
+    char *base = static_cast<char *>(scratch);
+    return cuda_status(moe::launch_route_fast(a, reinterpret_cast<unsigned *>(base), base + kRouteStatusBytes,
+                                              scratch_bytes - kRouteStatusBytes,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_dispatch(const moe_shape_t *shape, const moe_bf16_t *x, const int32_t *topk_idx,
                           int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_of_slot,
                           int32_t *slot_of_row, moe_bf16_t *x_perm, void *ws, size_t ws_bytes,
@@ -374,6 +406,19 @@ moe_status_t moe_combine(const moe_shape_t *shape, const moe_bf16_t *y_perm,
     return cuda_status(moe::launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Whether the layer routes by filter then verify: the tuning's choice, else
+// for more than 128 experts (where the direct kernels are slowest per token);
+// only where route_tc.cu supports the shape and the X_PERM region holds its
+// scratch.
+bool filter_verify_route(const moe_shape_t *s, const moe_tuning_t *t, const Layout &L)
+{
+    const int mode = t ? t->router : MOE_ROUTER_DEFAULT;
+    if (mode == MOE_ROUTER_DIRECT) return false;
+    if (mode == MOE_ROUTER_DEFAULT && s->E <= 128) return false;
+    return moe::route_fast_supported(s->T, s->d, s->E, s->top_k) &&
+           moe::route_fast_scratch_bytes(s->T, s->E) <= L.bytes[MOE_WS_X_PERM];
+}
+
 moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *tuning,
                                   const moe_bf16_t *x, const moe_bf16_t *w_router,
                                   const float *expert_bias, const moe_bf16_t *W1,
@@ -410,7 +455,11 @@ moe_status_t moe_layer_forward_ex(const moe_shape_t *shape, const moe_tuning_t *
     moe::RouteArgs ra{x, w_router, expert_bias, idx, gate, shape->T, shape->d, shape->E,
                       shape->top_k};
     if (!mark(0)) return MOE_ERR_CUDA;
-    cudaError_t err = moe::launch_route(ra, s);
+    cudaError_t err = filter_verify_route(shape, tuning, L)
+                          ? moe::launch_route_fast(ra, region<unsigned>(ws, L, MOE_WS_STATUS),
+                                                   region<void>(ws, L, MOE_WS_X_PERM),
+                                                   L.bytes[MOE_WS_X_PERM], s)
+                          : moe::launch_route(ra, s);
     if (err != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
 
     moe::DispatchArgs da{};
@@ -460,8 +509,9 @@ int moe_layer_kernel_launches(const moe_shape_t *shape, const moe_tuning_t *tuni
 {
     if (check_shape(shape) != MOE_OK || check_tuning(tuning) != MOE_OK) return 0;
     const bool fused = tuning && tuning->fused_combine;
+    const int route = filter_verify_route(shape, tuning, make_layout(shape, tuning)) ? 4 : 1;
     // route; count, scan, rank, copy; grouped GEMM; combine
-    return 1 + 4 + 1 + (fused ? 0 : 1);
+    return route + 4 + 1 + (fused ? 0 : 1);
 }
 
 moe_status_t moe_layer_forward_tuned(const moe_shape_t *shape, const moe_tuning_t *tuning,

@@ -18,7 +18,7 @@ enum : unsigned { kStatusBadExpert = 1u, kStatusBadOffsets = 1u, kStatusTimeout 
 enum : unsigned {
     kWhereProducerEmpty = 1, kWhereProducerDep = 2, kWhereMmaFull = 3, kWhereMmaTmemEmpty = 4,
     kWhereEpiTmemFull = 5, kWhereDispatch = 6, kWhereGemmOffsets = 7, kWhereCombine = 8,
-    kWhereMmaDrain = 9, kWhereLoadDrain = 10, kWhereTileQueue = 11
+    kWhereMmaDrain = 9, kWhereLoadDrain = 10, kWhereTileQueue = 11, kWhereRouteTc = 12
 };
 
 // Default wall-clock limit of any single wait (ns). The longest legitimate

@@ -85,6 +85,19 @@ typedef enum {
     MOE_ORIENT_TOKENS_N = 2
 } moe_orientation_t;
 
+/* How moe_layer_forward routes (step 1). Both give the same bits as moe_route:
+ * DIRECT sums every logit exactly (moe_route's kernels); FILTER_VERIFY computes
+ * every logit approximately on the tensor cores, bounds the error of both
+ * sums by |x_t| |w_e| (Cauchy-Schwarz), keeps the experts that can still be in
+ * the top k and sums exactly only those (tokens with too many candidates fall
+ * back to all experts). FILTER_VERIFY runs in four launches and uses the
+ * X_PERM region as scratch before the dispatch writes it. */
+typedef enum {
+    MOE_ROUTER_DEFAULT = 0,       /* FILTER_VERIFY when E > 128, else DIRECT */
+    MOE_ROUTER_DIRECT = 1,
+    MOE_ROUTER_FILTER_VERIFY = 2
+} moe_router_t;
+
 typedef struct {
     int schedule;   /* moe_schedule_t */
     int lead_rows;  /* D: minimum lead of Linear-1 over Linear-2 in scheduler rows; 0 = default;
@@ -134,6 +147,8 @@ typedef struct {
                            most 1024, never with fused_combine), 0 = default (mixed when
                            single-row experts are at least a quarter of the rows, else expert
                            order). Results are bit-identical either way. */
+    int router;         /* moe_router_t: how the layer routes; results are bit-identical either
+                           way. 0 = default (filter-then-verify for E > 128, else direct) */
 } moe_tuning_t;
 
 /* Human-readable name of a status code. Never NULL. */
@@ -187,6 +202,23 @@ moe_status_t moe_workspace_region_tuned(const moe_shape_t *shape, const moe_tuni
 moe_status_t moe_route(const moe_shape_t *shape, const moe_bf16_t *x, const moe_bf16_t *w_router,
                        const float *expert_bias, int32_t *topk_idx, float *topk_gate,
                        moe_stream_t stream);
+
+/* Bytes of device scratch moe_route_filtered needs for this shape; 0 for an
+ * invalid shape. */
+size_t moe_route_scratch_bytes(const moe_shape_t *shape);
+
+/* moe_route by filter then verify (moe_router_t MOE_ROUTER_FILTER_VERIFY):
+ * the same topk_idx and topk_gate bits as moe_route, in four launches that
+ * sum exactly only the experts that can still be in the top k.
+ * scratch: device buffer of at least moe_route_scratch_bytes, 256-byte
+ * aligned, owned by the caller; its first 16 bytes are a status word like the
+ * workspace's (zero before the call: allocate it zeroed, and
+ * moe_last_device_status(scratch, stream) reads and clears it). Calls that
+ * share a scratch buffer must not overlap on the GPU. d must be below 2^20
+ * (else MOE_ERR_UNSUPPORTED). */
+moe_status_t moe_route_filtered(const moe_shape_t *shape, const moe_bf16_t *x, const moe_bf16_t *w_router,
+                                const float *expert_bias, int32_t *topk_idx, float *topk_gate, void *scratch,
+                                size_t scratch_bytes, moe_stream_t stream);
 
 /* Step 2, dispatch (Cui et al. section 2.1 step 2): a stable counting sort of
  * the R token copies by expert, in (token, choice) order.
@@ -268,8 +300,10 @@ moe_status_t moe_combine(const moe_shape_t *shape, const moe_bf16_t *y_perm,
 
 /* The whole layer: route -> dispatch -> grouped SwiGLU GEMM -> combine, seven
  * kernel launches on one stream (route; count, scan, rank and copy for the
- * dispatch; the grouped GEMM; combine), no host synchronisation. Intermediates
- * (routing, permutation, x_perm, h, y_perm) stay in the workspace regions. */
+ * dispatch; the grouped GEMM; combine), ten when the route filters then
+ * verifies (moe_router_t: weight norms, candidates, exact candidates, full
+ * rows), no host synchronisation. Intermediates (routing, permutation, x_perm,
+ * h, y_perm) stay in the workspace regions. */
 moe_status_t moe_layer_forward(const moe_shape_t *shape, const moe_bf16_t *x,
                                const moe_bf16_t *w_router, const float *expert_bias,
                                const moe_bf16_t *W1, const moe_bf16_t *W3, const moe_bf16_t *W2,
@@ -277,8 +311,9 @@ moe_status_t moe_layer_forward(const moe_shape_t *shape, const moe_bf16_t *x,
                                moe_stream_t stream);
 
 /* Kernel launches one moe_layer_forward_tuned call makes for this shape and
- * tuning (NULL = defaults): route, the dispatch's count, scan, rank and row
- * copy, the grouped GEMM, and the combine unless fused_combine. 0 for an
+ * tuning (NULL = defaults): route (1, or 4 when it filters then verifies), the
+ * dispatch's count, scan, rank and row copy, the grouped GEMM, and the combine
+ * unless fused_combine. 0 for an
  * invalid shape or tuning; the layer makes no launch at all when T == 0. */
 int moe_layer_kernel_launches(const moe_shape_t *shape, const moe_tuning_t *tuning);
 

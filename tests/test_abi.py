@@ -200,11 +200,39 @@ def test_row_order_values_are_checked(lib):
 
 
 def test_layer_kernel_launches(lib):
-    """Host-side count of the layer's launches: route, four dispatch kernels,
-    the grouped GEMM and the combine (none when the combine is fused into the
-    GEMM)."""
+    """Host-side count of the layer's launches: route (one kernel, or four when
+    it filters then verifies: the default above 128 experts), four dispatch
+    kernels, the grouped GEMM and the combine (none when the combine is fused
+    into the GEMM)."""
     fine = moe.Shape(T=16384, d=4096, E=256, top_k=8, ffn=2048)
-    assert moe.layer_kernel_launches(fine) == 7
-    assert moe.layer_kernel_launches(fine, moe.Tuning(fused_combine=1)) == 6
+    assert moe.layer_kernel_launches(fine) == 10
+    assert moe.layer_kernel_launches(fine, moe.Tuning(fused_combine=1)) == 9
+    assert moe.layer_kernel_launches(fine, moe.Tuning(router=moe.ROUTER_DIRECT)) == 7
+    mid = moe.Shape(T=16384, d=2048, E=64, top_k=8, ffn=1024)
+    assert moe.layer_kernel_launches(mid) == 7
+    assert moe.layer_kernel_launches(mid, moe.Tuning(router=moe.ROUTER_FILTER_VERIFY)) == 10
+    at_128 = moe.Shape(T=1024, d=512, E=128, top_k=8, ffn=64)
+    assert moe.layer_kernel_launches(at_128) == 7
     bad = moe.Shape(T=10, d=12, E=4, top_k=2, ffn=16)  # d not a multiple of 8
     assert moe.layer_kernel_launches(bad) == 0
+    assert moe.layer_kernel_launches(fine, moe.Tuning(router=3)) == 0
+
+
+def test_route_filtered_host_checks(lib):
+    """moe_route_filtered rejects bad arguments before enqueuing anything."""
+    s = moe.Shape(T=64, d=64, E=4, top_k=2, ffn=64)
+    c = ctypes.byref(s.c())
+    nb = moe.route_scratch_bytes(s)
+    assert nb >= 256 + 64 * 64 + 64
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: a host check fails first
+    assert lib.moe_route_filtered(c, None, None, None, None, None, None, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_filtered(c, fake, fake, None, fake, fake, fake, nb - 1, None) == moe.MOE_ERR_WORKSPACE
+    odd = ctypes.c_void_p((1 << 20) + 16)  # 16-byte but not 256-byte aligned scratch
+    assert lib.moe_route_filtered(c, fake, fake, None, fake, fake, odd, nb, None) == moe.MOE_ERR_INVALID_ARG
+    empty = moe.Shape(T=0, d=64, E=4, top_k=2, ffn=64)
+    assert lib.moe_route_filtered(ctypes.byref(empty.c()), None, None, None, None, None, None, 0, None) == \
+        moe.MOE_OK
+    bad = moe.Shape(T=8, d=12, E=4, top_k=2, ffn=16)
+    assert moe.route_scratch_bytes(bad) == 0
+    assert lib.moe_route_filtered(ctypes.byref(bad.c()), fake, fake, None, fake, fake, fake, nb, None) == \
+        moe.MOE_ERR_INVALID_ARG
