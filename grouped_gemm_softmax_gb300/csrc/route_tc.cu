@@ -12,12 +12,11 @@
 //      staged x tiles. For token t and expert e the approximation and the
 //      exact sequential sum both lie within gamma * sum_i |x_ti w_ei| of the
 //      real dot product, and sum_i |x_ti w_ei| <= |x_t| |w_e| (Cauchy-Schwarz),
-//      so with B = 2 gamma |x_t| |w_e| (twice the bound, plus the roundings of
-//      the bias addition) the exact logit lies in [z~ - B, z~ + B]. An expert
-//      whose upper end is below the k-th largest lower end has k experts
-//      strictly above it and cannot be selected; the others ("candidates",
-//      about 16 of 256 on random data) are listed per token in ascending
-//      expert order.
+//      so with B = gamma |x_t| |w_e| (plus the roundings of the bias addition)
+//      the exact logit lies in [z~ - B, z~ + B]. An expert whose upper end is
+//      below the k-th largest lower end has k experts strictly above it and
+//      cannot be selected; the others ("candidates", about 15 of 256 on
+//      random data) are listed per token in ascending expert order.
 //   3. route_exact_kernel: CUDA cores sum the candidates' logits exactly, the
 //      same fused multiply-add per feature in ascending order as route.cu, and
 //      select among them (ties to the lower expert; the exponential sum paired
@@ -30,9 +29,12 @@
 // relative error at most u = 2^-24, so the sum is within gamma_d(u) *
 // sum |x w| of the real value (gamma_n(u) = n u / (1 - n u)). The tensor
 // core's internal order and rounding are not published; its accumulation is
-// taken as d steps each with relative error at most 2^-21 (8 u: room for
-// truncation and for aligning the products of a K step to the largest), the
-// norms are inflated by 1/256, and the interval is doubled on top.
+// taken as d steps each with relative error at most 2^-21 (8 u). Even if each
+// K = 16 step truncated all 16 products and the accumulator to 24 bits of the
+// largest of them, the error would stay under 17/16 * d * 2^-23 * sum |x w|,
+// a quarter of that allowance; on the fine-grained workload's inputs the
+// largest measured difference between the two sums is 0.0023 d 2^-24
+// sum |x w|. The norms are inflated by 1/256 for their own rounding.
 #include <float.h>
 #include <limits.h>
 #include <math.h>
@@ -306,7 +308,7 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             tc_fence_after();
             const long t = static_cast<long>(t0) + row;
             const float xn = sqrtf(sq * (1.0f + 1.0f / 256.0f));
-            const float bscale = 2.0f * p.gamma * xn;
+            const float bscale = p.gamma * xn;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
             const int nch = (p.E + 31) >> 5;
             // pass 1: the k-th largest lower end. top[] is kept descending and
@@ -383,11 +385,14 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
 // A block takes p.bt consecutive tokens and lists their (token, candidate)
 // pairs in groups of four of one token (a token's list is padded to a
 // multiple of four with copies of its first candidate, summed and dropped).
-// Thread i takes the i-th of NT nearly equal contiguous runs of groups, so
-// every thread does the same work whatever the candidate counts, and sums the
-// four pairs of a group as four interleaved chains sharing the token's x. The
-// block streams x and all E router weight rows through a ring of S chunks of
-// 64 features (unpadded 128-byte rows) with cp.async.
+// Consumer thread i takes the i-th of kExactConsumers nearly equal contiguous
+// runs of groups, so every thread does the same work whatever the candidate
+// counts, and sums the four pairs of a group as four interleaved chains
+// sharing the token's x. A producer warp streams x and all E router weight
+// rows through a ring of S chunks of 64 features (unpadded 128-byte rows) with
+// TMA; consumer warps wait on each chunk's full barrier and release a chunk
+// on its empty barrier when they no longer need it, with no block-wide
+// barrier between chunks.
 //
 // Lane l of a quarter warp (pk = l mod 8) walks the features in windows of 64
 // offset by 8 pk: window w covers features [64 (w - 1) + 8 pk, 64 w + 8 pk),
@@ -395,32 +400,55 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
 // the eight lanes of a quarter warp always read eight different bank groups,
 // whichever rows (candidate experts) they read. The windows tile the feature
 // axis in ascending order, so each logit is still one fused multiply-add per
-// feature in ascending order. A window needs chunks w - 1 and w resident; the
-// ring keeps S - 2 chunks in flight.
-constexpr int kExactThreads = 384;
+// feature in ascending order. A window needs chunks w - 1 and w resident, so
+// up to S - 2 chunks are in flight.
+constexpr int kExactConsumers = 384;
+constexpr int kExactThreads = kExactConsumers + 32;  // + the producer warp
+
+struct ExactBars {
+    uint64_t full[4];
+    uint64_t empty[4];
+    int abort;
+};
 
 __host__ __device__ constexpr size_t exact_tail_bytes(int BT)
 {
-    // zs [BT*64] f32, pexp [BT*64] u8, ptok [BT*16] u8, qbase [BT+1] i32
-    return static_cast<size_t>(BT) * kMaxCand * 5 + static_cast<size_t>(BT) * (kMaxCand / 4) +
-           (static_cast<size_t>(BT) + 1) * 4;
+    // zs [BT*64] f32, pexp [BT*64] u8, ptok [BT*16] u8, qbase [BT+1] i32, then
+    // the barriers (8-byte aligned)
+    return (static_cast<size_t>(BT) * kMaxCand * 5 + static_cast<size_t>(BT) * (kMaxCand / 4) +
+            (static_cast<size_t>(BT) + 1) * 4 + 7) / 8 * 8 +
+           sizeof(ExactBars);
 }
 
 template <int S>
-__global__ void __launch_bounds__(kExactThreads, 1) route_exact_kernel(const FastParams p)
+__global__ void __launch_bounds__(kExactThreads, 1)
+route_exact_kernel(const __grid_constant__ CUtensorMap tm_xr, const __grid_constant__ CUtensorMap tm_wr,
+                   const FastParams p)
 {
-    extern __shared__ __align__(128) uint8_t ex_raw[];
+    extern __shared__ uint8_t ex_raw[];
+    uint8_t *ring_p = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ex_raw) + 1023) & ~uintptr_t(1023));
     const int NT = blockDim.x, BT = p.bt, E = p.E;
-    const int rows = BT + E;
-    const uint32_t stage_bytes = static_cast<uint32_t>(rows) * 128u;
-    const uint32_t ring = smem_u32(ex_raw);
-    float *zs = reinterpret_cast<float *>(ex_raw + S * stage_bytes);          // [BT*64] per pair
+    const uint32_t stage_bytes = static_cast<uint32_t>(BT + E) * 128u;
+    const uint32_t ring = smem_u32(ring_p);
+    float *zs = reinterpret_cast<float *>(ring_p + S * stage_bytes);          // [BT*64] per pair
     uint8_t *pexp = reinterpret_cast<uint8_t *>(zs + BT * kMaxCand);         // [BT*64] per pair
     uint8_t *ptok = pexp + BT * kMaxCand;                                     // [BT*16] per group
     int *qbase = reinterpret_cast<int *>(ptok + BT * (kMaxCand / 4));         // [BT+1]
+    ExactBars &bars = *reinterpret_cast<ExactBars *>(
+        (reinterpret_cast<uintptr_t>(qbase + BT + 1) + 7) & ~uintptr_t(7));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, pk = tid & 7;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], kExactConsumers / 32);
+        }
+        bars.abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tm_xr);
+        tma_prefetch_desc(&tm_wr);
+    }
     pdl_wait();
     pdl_trigger();
-    const int tid = threadIdx.x, pk = tid & 7;
     const long t0 = static_cast<long>(blockIdx.x) * BT;
     // groups per token, their exclusive scan (one warp), then the pair lists
     if (tid < 32) {
@@ -457,84 +485,100 @@ __global__ void __launch_bounds__(kExactThreads, 1) route_exact_kernel(const Fas
         for (int q = 0; q < nq; ++q) ptok[q0 + q] = static_cast<uint8_t>(j);
     }
     __syncthreads();
-    const int Q = qbase[BT];
-    const int g_begin = static_cast<int>((static_cast<long>(Q) * tid) / NT);
-    const int g_end = static_cast<int>((static_cast<long>(Q) * (tid + 1)) / NT);
     const int nchunks = (p.d + 63) / 64, nsub = p.d / 8;
-    auto issue = [&](int ch) {
-        const uint32_t st = ring + static_cast<uint32_t>(ch % S) * stage_bytes;
-        const int col0 = ch * 64;
-        for (int v = tid; v < rows * 8; v += NT) {
-            const int r = v >> 3, c8 = (v & 7) * 8;
-            const bool is_x = r < BT;
-            const long grow = is_x ? t0 + r : static_cast<long>(r - BT);
-            const bool ok = col0 + c8 < p.d && (!is_x || grow < p.T);
-            const uint16_t *src = ok ? (is_x ? p.x : p.wr) + grow * p.d + col0 + c8 : p.x;
-            cp_async16(st + static_cast<uint32_t>(v) * 16u, src, ok);
-        }
-    };
-#pragma unroll
-    for (int ch = 0; ch < S - 2; ++ch) {
-        if (ch < nchunks) issue(ch);
-        cp_commit();
-    }
-    for (int w = 0; w <= nchunks; ++w) {
-        cp_wait<S - 3>();
-        __syncthreads();  // chunk w landed for every thread; window w - 1 is done everywhere
-        {
-            const int ch = w + S - 2;  // into the slot of chunk w - 2
-            if (ch < nchunks) issue(ch);
-            cp_commit();
-        }
-        if (g_begin == g_end) continue;
-        const int cl = w - 1;
-        const uint32_t lo = ring + static_cast<uint32_t>((cl + S) % S) * stage_bytes;
-        const uint32_t hi = ring + static_cast<uint32_t>(w % S) * stage_bytes;
-        uint32_t off[8];
-        unsigned vmask = 0;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const int q = pk + jj;
-            const int g = 8 * cl + q;
-            off[jj] = (q < 8 ? lo : hi) + static_cast<uint32_t>((q & 7) << 4);
-            vmask |= (g >= 0 && g < nsub ? 1u : 0u) << jj;
-        }
-        uint4 xr[8];
-        int cur = -1;
-        for (int gq = g_begin; gq < g_end; ++gq) {
-            const int tok = ptok[gq];
-            if (tok != cur) {
-                cur = tok;
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    xr[jj] = ((vmask >> jj) & 1u) ? lds128(off[jj] + static_cast<uint32_t>(tok) * 128u)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
+    volatile int *abort_flag = &bars.abort;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            for (int ch = 0; ch < nchunks; ++ch) {
+                const int s = ch % S;
+                const uint32_t ph = static_cast<uint32_t>(ch / S) & 1u;
+                if (!mbar_wait(&bars.empty[s], ph ^ 1u, abort_flag, p.status, kWhereRouteTc, 7u, kCandWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars.full[s], stage_bytes);
+                const uint32_t bar = smem_u32(&bars.full[s]);
+                tma_load_2d<1>(&tm_xr, bar, ring_p + s * stage_bytes, ch * 64, static_cast<int>(t0));
+                tma_load_2d<1>(&tm_wr, bar, ring_p + s * stage_bytes + BT * 128, ch * 64, 0);
+                ++issued;
             }
-            const uchar4 ex4 = *reinterpret_cast<const uchar4 *>(pexp + 4 * gq);
-            const uint32_t eo[4] = {static_cast<uint32_t>(BT + ex4.x) * 128u, static_cast<uint32_t>(BT + ex4.y) * 128u,
-                                    static_cast<uint32_t>(BT + ex4.z) * 128u, static_cast<uint32_t>(BT + ex4.w) * 128u};
-            float4 a = *reinterpret_cast<const float4 *>(zs + 4 * gq);
+            if (!ok) {
+                for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+                    if (!mbar_wait_drain(&bars.full[i % S], static_cast<uint32_t>(i / S) & 1u, kDrainNs))
+                        report_failure(p.status, kStatusTimeout, kWhereRouteTc, 9u);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int ctid = tid - 32;
+        const int Q = qbase[BT];
+        const int g_begin = static_cast<int>((static_cast<long>(Q) * ctid) / kExactConsumers);
+        const int g_end = static_cast<int>((static_cast<long>(Q) * (ctid + 1)) / kExactConsumers);
+        for (int w = 0; w <= nchunks; ++w) {
+            if (w < nchunks) {
+                const bool ready = mbar_wait(&bars.full[w % S], static_cast<uint32_t>(w / S) & 1u, abort_flag,
+                                             p.status, kWhereRouteTc, 8u, kCandWaitNs);
+                if (!__all_sync(0xffffffffu, ready)) break;
+            }
+            if (g_begin < g_end) {
+                const int cl = w - 1;
+                const uint32_t lo = ring + static_cast<uint32_t>((cl + S) % S) * stage_bytes;
+                const uint32_t hi = ring + static_cast<uint32_t>(w % S) * stage_bytes;
+                uint32_t off[8];
+                unsigned vmask = 0;
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                if ((vmask >> jj) & 1u) {
-                    const uint4 w0 = lds128(off[jj] + eo[0]);
-                    const uint4 w1 = lds128(off[jj] + eo[1]);
-                    const uint4 w2 = lds128(off[jj] + eo[2]);
-                    const uint4 w3 = lds128(off[jj] + eo[3]);
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int q = pk + jj;
+                    const int g = 8 * cl + q;
+                    off[jj] = (q < 8 ? lo : hi) + static_cast<uint32_t>((q & 7) << 4);
+                    vmask |= (g >= 0 && g < nsub ? 1u : 0u) << jj;
+                }
+                uint4 xr[8];
+                int cur = -1;
+                for (int gq = g_begin; gq < g_end; ++gq) {
+                    const int tok = ptok[gq];
+                    if (tok != cur) {
+                        cur = tok;
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const uint16_t xv = half_of(xr[jj], g);
-                        a.x = fma_bf16x(xv, half_of(w0, g), a.x);
-                        a.y = fma_bf16x(xv, half_of(w1, g), a.y);
-                        a.z = fma_bf16x(xv, half_of(w2, g), a.z);
-                        a.w = fma_bf16x(xv, half_of(w3, g), a.w);
+                        for (int jj = 0; jj < 8; ++jj)
+                            xr[jj] = ((vmask >> jj) & 1u) ? lds128(off[jj] + static_cast<uint32_t>(tok) * 128u)
+                                                          : make_uint4(0u, 0u, 0u, 0u);
                     }
+                    const uchar4 ex4 = *reinterpret_cast<const uchar4 *>(pexp + 4 * gq);
+                    const uint32_t eo[4] = {static_cast<uint32_t>(BT + ex4.x) * 128u,
+                                            static_cast<uint32_t>(BT + ex4.y) * 128u,
+                                            static_cast<uint32_t>(BT + ex4.z) * 128u,
+                                            static_cast<uint32_t>(BT + ex4.w) * 128u};
+                    float4 a = *reinterpret_cast<const float4 *>(zs + 4 * gq);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        if ((vmask >> jj) & 1u) {
+                            const uint4 w0 = lds128(off[jj] + eo[0]);
+                            const uint4 w1 = lds128(off[jj] + eo[1]);
+                            const uint4 w2 = lds128(off[jj] + eo[2]);
+                            const uint4 w3 = lds128(off[jj] + eo[3]);
+#pragma unroll
+                            for (int g = 0; g < 8; ++g) {
+                                const uint16_t xv = half_of(xr[jj], g);
+                                a.x = fma_bf16x(xv, half_of(w0, g), a.x);
+                                a.y = fma_bf16x(xv, half_of(w1, g), a.y);
+                                a.z = fma_bf16x(xv, half_of(w2, g), a.z);
+                                a.w = fma_bf16x(xv, half_of(w3, g), a.w);
+                            }
+                        }
+                    }
+                    *reinterpret_cast<float4 *>(zs + 4 * gq) = a;
                 }
             }
-            *reinterpret_cast<float4 *>(zs + 4 * gq) = a;
+            __syncwarp();
+            if (w >= 1 && lane == 0) mbar_arrive(&bars.empty[(w - 1) % S]);  // chunk w - 1 is done here
         }
     }
     __syncthreads();
+    if (*abort_flag) return;
     // selection: one thread per token over its n candidates (pairs 4 q0 ..)
     for (int j = tid; j < BT; j += NT) {
         const long t = t0 + j;
@@ -685,7 +729,7 @@ constexpr size_t cand_smem_bytes()
 
 size_t exact_smem_bytes(int S, int BT, int E)
 {
-    return static_cast<size_t>(S) * (BT + E) * 128 + exact_tail_bytes(BT);
+    return 1024 + static_cast<size_t>(S) * (BT + E) * 128 + exact_tail_bytes(BT);
 }
 
 struct ExactPlan {
@@ -705,7 +749,7 @@ ExactPlan exact_plan(long T, int E, int sms)
     return pl;
 }
 
-bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer)
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer, bool swizzle)
 {
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {inner * 2};
@@ -714,8 +758,8 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, u
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // gamma_n(u) = n u / (1 - n u), rounded up to float
@@ -771,8 +815,10 @@ cudaError_t launch_route_fast(const RouteArgs &a, unsigned *status, void *scratc
                              static_cast<float>(INFINITY));
     p.abs_eps = static_cast<float>(std::ldexp(static_cast<double>(a.d), -120));
 
-    CUtensorMap tm_x, tm_w;
-    if (!make_map(&tm_x, a.x, a.d, a.T, kCandM) || !make_map(&tm_w, a.wr, a.d, a.E, p.npad))
+    // swizzled tiles for the candidate kernel's MMAs, plain rows for the exact kernel
+    CUtensorMap tm_x, tm_w, tm_xr, tm_wr;
+    if (!make_map(&tm_x, a.x, a.d, a.T, kCandM, true) || !make_map(&tm_w, a.wr, a.d, a.E, p.npad, true) ||
+        !make_map(&tm_xr, a.x, a.d, a.T, pl.bt, false) || !make_map(&tm_wr, a.wr, a.d, a.E, a.E, false))
         return cudaErrorInvalidValue;
 
     struct CandTag {};
@@ -808,8 +854,8 @@ cudaError_t launch_route_fast(const RouteArgs &a, unsigned *status, void *scratc
     if (e != cudaSuccess) return e;
     const dim3 eg((a.T + pl.bt - 1) / pl.bt);
     const size_t esm = exact_smem_bytes(pl.stages, pl.bt, a.E);
-    e = pl.stages == 4 ? launch_pdl(route_exact_kernel<4>, eg, dim3(kExactThreads), esm, s, p)
-                       : launch_pdl(route_exact_kernel<3>, eg, dim3(kExactThreads), esm, s, p);
+    e = pl.stages == 4 ? launch_pdl(route_exact_kernel<4>, eg, dim3(kExactThreads), esm, s, tm_xr, tm_wr, p)
+                       : launch_pdl(route_exact_kernel<3>, eg, dim3(kExactThreads), esm, s, tm_xr, tm_wr, p);
     if (e != cudaSuccess) return e;
     const int fg = a.T < sms ? a.T : sms;
     return launch_pdl(route_full_kernel, dim3(fg), dim3(kFullThreads), static_cast<size_t>(a.d) * 2, s, p);
