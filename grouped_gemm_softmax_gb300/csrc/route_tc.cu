@@ -50,7 +50,10 @@ namespace {
 constexpr int kCandM = 128;        // tokens per CTA of the candidate kernel (the MMA's M)
 constexpr int kCandK = 64;         // features per stage: one 128-byte swizzle row of bf16
 constexpr int kCandStages = 4;
-constexpr int kCandThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kCandSlices = 4;     // epilogue warps per 32-lane quarter of tensor memory
+constexpr int kCandEpiWarps = 4 * kCandSlices;
+constexpr int kCandThreads = 64 + 32 * kCandEpiWarps;  // warp 0 TMA, warp 1 MMA, then the epilogue
+constexpr int kCandSliceCols = 256 / kCandSlices;
 constexpr int kCandATile = kCandM * kCandK * 2;
 constexpr int kCandBTile = 256 * kCandK * 2;
 constexpr int kMaxCand = 64;       // candidates kept per token
@@ -109,18 +112,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Softmax denominator of the k selected logits (ev[j] = exp(z_j - z_0), zero
 // past k), summed in the pairing of a 32-lane xor butterfly over lanes j < k.
 __device__ __forceinline__ float butterfly_den(const float (&ev)[16])
@@ -167,11 +158,30 @@ struct CandSmem {
     uint64_t empty[kCandStages];
     uint64_t tfull;
     uint64_t drain;
+    uint64_t epi;  // the epilogue warps' barrier: one arrival per warp, bounded waits
     uint32_t tmem_base;
     int abort;
     float wn[256];  // |w_e| (inflated)
     float bias[256];
+    // per token row and column slice: partial squared norm, the slice's
+    // kMaxTopK largest lower ends, its candidate count and sanity
+    float sq[kCandSlices][kCandM];
+    float top[kCandSlices][kCandM][kMaxTopK];
+    int ncand[kCandSlices][kCandM];
+    int insane[kCandSlices][kCandM];
 };
+
+// Barrier among the candidate kernel's epilogue warps on an mbarrier (phase
+// parity `ph`): each warp reconverges, lane 0 arrives, every lane waits with
+// the usual limit. Returns false (the CTA's abort flag raised) if it gave up.
+__device__ __forceinline__ bool epi_barrier(CandSmem &c, uint32_t ph, volatile int *abort_flag, unsigned *status,
+                                            int lane)
+{
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.epi);
+    const bool ok = mbar_wait(&c.epi, ph, abort_flag, status, kWhereRouteTc, 10u + ph, kCandWaitNs);
+    return __all_sync(0xffffffffu, ok);
+}
 
 __global__ void __launch_bounds__(kCandThreads, 1)
 route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -187,10 +197,11 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < kCandStages; ++s) {
             mbar_init(&c.full[s], 1);
-            mbar_init(&c.empty[s], 1 + 4);  // the MMAs' commit and the four epilogue warps
+            mbar_init(&c.empty[s], 1 + kCandEpiWarps);  // the MMAs' commit and every epilogue warp
         }
         mbar_init(&c.tfull, 1);
         mbar_init(&c.drain, 1);
+        mbar_init(&c.epi, kCandEpiWarps);
         c.abort = 0;
         fence_barrier_init();
     }
@@ -274,11 +285,14 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         }
         __syncwarp();
     } else {
-        // During the mainloop: the squared norm of this lane's token row from
-        // each staged x tile. Lane i reads the row's 16-byte pieces starting at
-        // position i mod 8, so the eight lanes of each quarter warp hit eight
-        // different bank groups; the order of the pieces does not matter here.
-        const int q = warp & 3;  // this warp's 32 lanes of tensor memory
+        // Epilogue warp (quarter q, slice sl): token rows 32 q .. 32 q + 31 (one
+        // per lane, the tensor-memory lanes this warp may read) and experts
+        // [64 sl, 64 sl + 64). During the mainloop it adds the squares of its
+        // rows' 16-byte pieces sl and sl + kCandSlices of each staged x tile
+        // (in any order: the norm only bounds the error); lane i reads its
+        // pieces at swizzled positions that differ across the quarter warp.
+        const int q = warp & 3;
+        const int sl = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         float sq = 0.0f;
         bool ok = true;
@@ -292,8 +306,9 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             }
             const uint8_t *r = sA + s * kCandATile + row * (kCandK * 2);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(r + (((j + lane) & 7) << 4));
+            for (int j = 0; j < 8 / kCandSlices; ++j) {
+                const int piece = sl + j * kCandSlices;
+                const uint4 v = *reinterpret_cast<const uint4 *>(r + ((piece ^ (row & 7)) << 4));
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                     const float f = bf16f(half_of(v, g));
@@ -303,71 +318,143 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.empty[s]);
         }
-        const bool got = ok && mbar_wait(&c.tfull, 0u, abort_flag, p.status, kWhereRouteTc, 4u, kCandWaitNs);
-        if (__all_sync(0xffffffffu, got)) {
+        // a wait that gave up raised the CTA's abort flag before this barrier,
+        // so every epilogue warp takes the same branch after it
+        if (ok) mbar_wait(&c.tfull, 0u, abort_flag, p.status, kWhereRouteTc, 4u, kCandWaitNs);
+        c.sq[sl][row] = sq;
+        if (epi_barrier(c, 0u, abort_flag, p.status, lane) && *abort_flag == 0) {
             tc_fence_after();
             const long t = static_cast<long>(t0) + row;
-            const float xn = sqrtf(sq * (1.0f + 1.0f / 256.0f));
+            float sqa = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kCandSlices; ++i) sqa += c.sq[i][row];
+            const float xn = sqrtf(sqa * (1.0f + 1.0f / 256.0f));
             const float bscale = p.gamma * xn;
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            const int nch = (p.E + 31) >> 5;
-            // pass 1: the k-th largest lower end. top[] is kept descending and
-            // starts with kMaxTopK - k entries of +inf, so its last entry is
-            // the k-th largest value inserted.
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + sl * kCandSliceCols;
+            const int e0 = sl * kCandSliceCols;
+            // pass 1: this slice's kMaxTopK largest lower ends, descending
+            // (starting with kMaxTopK - k entries of +inf, so the last entry
+            // is the k-th largest inserted)
             float top[kMaxTopK];
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j) top[j] = j < kMaxTopK - p.k ? INFINITY : -INFINITY;
             float kth = -INFINITY;
-            bool sane = isfinite(xn);
-            for (int ch = 0; ch < nch; ++ch) {
-                uint32_t v[32];
-                tmem_load_32cols(taddr + ch * 32, v);
+            bool sane = true;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int e = ch * 32 + j;
-                    if (e < p.E) {
-                        const float z = __uint_as_float(v[j]) + c.bias[e];
-                        const float b = bscale * c.wn[e] + 4.8e-7f * fabsf(z) + p.abs_eps;
-                        // b < 1e30 keeps every partial sum of both logits far from overflow
-                        sane = sane && isfinite(z) && b < 1.0e30f;
-                        const float lo = z - b;
-                        if (lo > kth) {
-                            float cur = lo;
+            for (int ch = 0; ch < kCandSliceCols / 32; ++ch) {
+                if (e0 + ch * 32 < p.E) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_load_32cols(taddr + ch * 32, v);
 #pragma unroll
-                            for (int i = 0; i < kMaxTopK; ++i) {
-                                const float big = fmaxf(top[i], cur);
-                                cur = fminf(top[i], cur);
-                                top[i] = big;
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = e0 + ch * 32 + j;
+                        if (e < p.E) {
+                            const float z = __uint_as_float(v[j]) + c.bias[e];
+                            const float b = fmaf(bscale, c.wn[e], fmaf(4.8e-7f, fabsf(z), p.abs_eps));
+                            // NaN fails both comparisons; b < 1e30 keeps every
+                            // partial sum of both logits far from overflow
+                            sane = sane && fabsf(z) < 3.0e38f && b < 1.0e30f;
+                            const float lo = z - b;
+                            if (lo > kth) {
+                                float cur = lo;
+#pragma unroll
+                                for (int i = 0; i < kMaxTopK; ++i) {
+                                    const float big = fmaxf(top[i], cur);
+                                    cur = fminf(top[i], cur);
+                                    top[i] = big;
+                                }
+                                kth = top[kMaxTopK - 1];
                             }
-                            kth = top[kMaxTopK - 1];
                         }
                     }
                 }
             }
-            // pass 2: every expert whose upper end reaches the k-th lower end
-            int n = 0;
-            for (int ch = 0; ch < nch; ++ch) {
-                uint32_t v[32];
-                tmem_load_32cols(taddr + ch * 32, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int e = ch * 32 + j;
-                    if (e < p.E && t < p.T) {
-                        const float z = __uint_as_float(v[j]) + c.bias[e];
-                        const float b = bscale * c.wn[e] + 4.8e-7f * fabsf(z) + p.abs_eps;
-                        if (z + b >= kth) {
-                            if (n < kMaxCand) p.cand[t * kMaxCand + n] = static_cast<uint8_t>(e);
-                            ++n;
+            for (int j = 0; j < kMaxTopK; ++j) c.top[sl][row][j] = top[j];
+            // a non-finite or huge logit or bound sends the token to the full path
+            c.insane[sl][row] = !sane || !(xn < 3.0e38f);
+            const bool b2 = epi_barrier(c, 1u, abort_flag, p.status, lane);
+            // the k-th largest lower end over all slices (each slice's list ends
+            // with its k largest; the entries before them are padding)
+#pragma unroll 1
+            for (int o = 0; o < kCandSlices; ++o) {
+                if (o == sl) continue;
+#pragma unroll 1
+                for (int jj = kMaxTopK - p.k; jj < kMaxTopK; ++jj) {
+                    const float lo = c.top[o][row][jj];
+                    if (lo > kth) {
+                        float cur = lo;
+#pragma unroll
+                        for (int i = 0; i < kMaxTopK; ++i) {
+                            const float big = fmaxf(top[i], cur);
+                            cur = fminf(top[i], cur);
+                            top[i] = big;
+                        }
+                        kth = top[kMaxTopK - 1];
+                    }
+                }
+            }
+            // pass 2: this slice's experts whose upper end reaches it, counted,
+            // then written after the earlier slices' candidates
+            int n = 0;
+#pragma unroll
+            for (int ch = 0; ch < kCandSliceCols / 32; ++ch) {
+                if (e0 + ch * 32 < p.E) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_load_32cols(taddr + ch * 32, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = e0 + ch * 32 + j;
+                        if (e < p.E) {
+                            const float z = __uint_as_float(v[j]) + c.bias[e];
+                            const float b = fmaf(bscale, c.wn[e], fmaf(4.8e-7f, fabsf(z), p.abs_eps));
+                            n += z + b >= kth ? 1 : 0;
                         }
                     }
                 }
             }
-            if (t < p.T) {
-                if (!sane || n > kMaxCand || n < p.k) {
+            c.ncand[sl][row] = n;
+            const bool b3 = epi_barrier(c, 0u, abort_flag, p.status, lane);
+            int base_n = 0, total = 0, bad = !(b2 && b3);
+#pragma unroll
+            for (int i = 0; i < kCandSlices; ++i) {
+                const int ni = c.ncand[i][row];
+                base_n += i < sl ? ni : 0;
+                total += ni;
+                bad |= c.insane[i][row];
+            }
+            const bool over = bad || total > kMaxCand || total < p.k;
+            // the tensor-memory loads are warp-wide: the whole warp runs this
+            // pass when any lane writes, and only the writing lanes store
+            const bool write = !over && n > 0 && t < p.T;
+            if (__any_sync(0xffffffffu, write)) {
+                int m = base_n;
+#pragma unroll
+                for (int ch = 0; ch < kCandSliceCols / 32; ++ch) {
+                    if (e0 + ch * 32 < p.E) {
+                        uint32_t v[32];
+                        __syncwarp();
+                        tmem_load_32cols(taddr + ch * 32, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int e = e0 + ch * 32 + j;
+                            if (e < p.E) {
+                                const float z = __uint_as_float(v[j]) + c.bias[e];
+                                const float b = fmaf(bscale, c.wn[e], fmaf(4.8e-7f, fabsf(z), p.abs_eps));
+                                if (write && z + b >= kth) p.cand[t * kMaxCand + m++] = static_cast<uint8_t>(e);
+                            }
+                        }
+                    }
+                }
+            }
+            if (sl == 0 && t < p.T) {
+                if (over) {
                     p.cnt[t] = kOverflow;
                     p.ovf[atomicAdd(p.novf, 1u)] = static_cast<int32_t>(t);
                 } else {
-                    p.cnt[t] = static_cast<uint8_t>(n);
+                    p.cnt[t] = static_cast<uint8_t>(total);
                 }
             }
         }
