@@ -232,27 +232,24 @@ route_cand_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
         if (lane == 0) {
             const uint32_t bytes = kCandATile + static_cast<uint32_t>(p.npad) * kCandK * 2;
             int issued = 0;
-            bool ok = true;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % kCandStages;
                 const uint32_t ph = static_cast<uint32_t>(kb / kCandStages) & 1u;
-                if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag, p.status, kWhereRouteTc, 1u, kCandWaitNs)) {
-                    ok = false;
+                if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag, p.status, kWhereRouteTc, 1u, kCandWaitNs))
                     break;
-                }
                 mbar_arrive_expect_tx(&c.full[s], bytes);
                 const uint32_t bar = smem_u32(&c.full[s]);
                 tma_load_2d<1>(&tm_x, bar, sA + s * kCandATile, kb * kCandK, t0);
                 tma_load_2d<1>(&tm_w, bar, sB + s * kCandBTile, kb * kCandK, 0);
                 ++issued;
             }
-            if (!ok) {
-                // only the last kCandStages loads can still be in flight
-                for (int i = issued > kCandStages ? issued - kCandStages : 0; i < issued; ++i)
-                    if (!mbar_wait_drain(&c.full[i % kCandStages], static_cast<uint32_t>(i / kCandStages) & 1u,
-                                         kDrainNs))
-                        report_failure(p.status, kStatusTimeout, kWhereRouteTc, 5u);
-            }
+            // every load issued has landed before the CTA can exit, also when a
+            // consumer gave up waiting for it (only the last kCandStages can
+            // still be in flight; their phases have completed otherwise)
+            for (int i = issued > kCandStages ? issued - kCandStages : 0; i < issued; ++i)
+                if (!mbar_wait_drain(&c.full[i % kCandStages], static_cast<uint32_t>(i / kCandStages) & 1u,
+                                     kDrainNs))
+                    report_failure(p.status, kStatusTimeout, kWhereRouteTc, 5u);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -578,25 +575,22 @@ route_exact_kernel(const __grid_constant__ CUtensorMap tm_xr, const __grid_const
     if (warp == 0) {
         if (lane == 0) {
             int issued = 0;
-            bool ok = true;
             for (int ch = 0; ch < nchunks; ++ch) {
                 const int s = ch % S;
                 const uint32_t ph = static_cast<uint32_t>(ch / S) & 1u;
-                if (!mbar_wait(&bars.empty[s], ph ^ 1u, abort_flag, p.status, kWhereRouteTc, 7u, kCandWaitNs)) {
-                    ok = false;
+                if (!mbar_wait(&bars.empty[s], ph ^ 1u, abort_flag, p.status, kWhereRouteTc, 7u, kCandWaitNs))
                     break;
-                }
                 mbar_arrive_expect_tx(&bars.full[s], stage_bytes);
                 const uint32_t bar = smem_u32(&bars.full[s]);
                 tma_load_2d<1>(&tm_xr, bar, ring_p + s * stage_bytes, ch * 64, static_cast<int>(t0));
                 tma_load_2d<1>(&tm_wr, bar, ring_p + s * stage_bytes + BT * 128, ch * 64, 0);
                 ++issued;
             }
-            if (!ok) {
-                for (int i = issued > S ? issued - S : 0; i < issued; ++i)
-                    if (!mbar_wait_drain(&bars.full[i % S], static_cast<uint32_t>(i / S) & 1u, kDrainNs))
-                        report_failure(p.status, kStatusTimeout, kWhereRouteTc, 9u);
-            }
+            // every load issued has landed before the CTA can exit (see the
+            // candidate kernel's producer)
+            for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+                if (!mbar_wait_drain(&bars.full[i % S], static_cast<uint32_t>(i / S) & 1u, kDrainNs))
+                    report_failure(p.status, kStatusTimeout, kWhereRouteTc, 9u);
         }
         __syncwarp();
     } else {

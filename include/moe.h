@@ -345,7 +345,9 @@ moe_status_t moe_last_device_status(void *ws, moe_stream_t stream);
 
 /* Detail words of the last device failure that moe_last_device_status read on
  * the calling thread (valid after it returned non-OK there): where (kernel/role
- * code), block index, detail. */
+ * code: 1-5 grouped-GEMM pipeline waits, 6 dispatch, 7 GEMM offsets, 8 fused
+ * combine, 9-10 GEMM drains, 11 tile queue, 12 filter-then-verify router),
+ * block index, detail. */
 void moe_last_device_detail(uint32_t *where, uint32_t *block, uint32_t *detail);
 
 #ifdef __cplusplus

@@ -236,3 +236,23 @@ def test_route_filtered_host_checks(lib):
     assert moe.route_scratch_bytes(bad) == 0
     assert lib.moe_route_filtered(ctypes.byref(bad.c()), fake, fake, None, fake, fake, fake, nb, None) == \
         moe.MOE_ERR_INVALID_ARG
+
+
+def test_layer_routes_directly_when_x_perm_cannot_hold_the_scratch(lib):
+    """The filter-then-verify router keeps its scratch in the X_PERM region
+    (T*k*d*2 bytes); with k*d*2 below its ~69 bytes per token the layer
+    routes directly instead."""
+    roomy = moe.Shape(T=1000, d=64, E=200, top_k=1, ffn=16)
+    tight = moe.Shape(T=1000, d=8, E=200, top_k=1, ffn=16)
+    assert moe.layer_kernel_launches(roomy) == 10
+    assert moe.layer_kernel_launches(tight) == 7
+    assert moe.layer_kernel_launches(tight, moe.Tuning(router=moe.ROUTER_FILTER_VERIFY)) == 7
+
+
+def test_route_filtered_rejects_a_huge_feature_dimension(lib):
+    s = moe.Shape(T=1, d=1 << 20, E=4, top_k=2, ffn=8)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the shape check fails first
+    nb = moe.route_scratch_bytes(s)
+    assert nb > 0
+    assert lib.moe_route_filtered(ctypes.byref(s.c()), fake, fake, None, fake, fake, fake, nb, None) == \
+        moe.MOE_ERR_UNSUPPORTED
